@@ -1,0 +1,136 @@
+"""FP8 per-token x per-channel GEMM on the tensor cores vs the oracle's fp64
+dequantized product (through the C ABI).
+
+The GEMM's inputs are the oracle's own codes and scales (uploaded), so the
+comparison isolates the GEMM; one end-to-end case runs the GPU quantizers
+first (their codes are bit-exact with the oracle's, tested elsewhere).
+Tolerance: |y - y_ref| <= 1e-3 * sum_k |x^_k w^_k| + 1 bf16 ulp of y_ref.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import codecs as C
+from oracle import quant as Q
+from oracle import gemm as G
+from gpu_util import lpq, dev_bf16, dev, host, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_operands(M, N, K, seed):
+    xb = synth.activations(M, K, seed, n_outlier=max(1, K // 1000), lo=50, hi=500)
+    wb = synth.weights(N, K, seed + 1)
+    qx, sx = Q.fp8_per_row(synth.f32_from_bf16_bits(xb))
+    qw, sw = Q.fp8_per_row(synth.f32_from_bf16_bits(wb))
+    return xb, wb, qx, sx, qw, sw
+
+
+def _ref(qx, sx, qw, sw):
+    y, b = G.matmul_ref(Q.fp8_dequant(qx, sx[:, None]), Q.fp8_dequant(qw, sw[:, None]))
+    return y, b
+
+
+def _run(L, qx, sx, qw, sw, M, N, K, workspace=False, static=False):
+    A, B = dev(qx), dev(qw)
+    sa, sb = dev(sx), dev(sw)
+    ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K) if workspace else None
+    gran = L.GRAN_TENSOR_STATIC if static else L.GRAN_ROW
+    Y = L.gemm_scaled(L.FMT_FP8, gran, L.GRAN_ROW, A, B, sa, sb, M=M, N=N, K=K, workspace=ws)
+    torch.cuda.synchronize()
+    return host(Y), ws
+
+
+SHAPES = [
+    (16, 256, 256),        # the tiny W8A8 configuration
+    (1, 128, 128), (1, 4096, 4096), (5, 200, 336), (16, 6144, 4096), (64, 4096, 14336),
+    (200, 1000, 1024), (256, 4096, 4096), (300, 520, 4096), (1000, 4096, 2048), (517, 384, 144),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("workspace", [False, True])
+def test_fp8_rowscale_gemm(M, N, K, workspace):
+    L = lpq()
+    _, _, qx, sx, qw, sw = _oracle_operands(M, N, K, 1000 + M + N + K)
+    y, ws = _run(L, qx, sx, qw, sw, M, N, K, workspace=workspace)
+    yr, b = _ref(qx, sx, qw, sw)
+    ok, worst = G.check(bf16_to_f64(y), yr, b)
+    assert ok.all(), f"{(~ok).sum()} outputs out of tolerance, worst ratio {worst:.3g}"
+
+
+def test_fp8_workspace_counters_return_to_zero():
+    L = lpq()
+    M, N, K = 1, 4096, 4096
+    _, _, qx, sx, qw, sw = _oracle_operands(M, N, K, 77)
+    ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
+    assert ws.numel() > 16, "expected a split-K plan for a single-token 4096x4096 GEMM"
+    yr, b = _ref(qx, sx, qw, sw)
+    for _ in range(3):
+        A, B = dev(qx), dev(qw)
+        Y = L.gemm_scaled(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, A, B, dev(sx), dev(sw), M=M, N=N, K=K, workspace=ws)
+        torch.cuda.synchronize()
+        ok, worst = G.check(bf16_to_f64(host(Y)), yr, b)
+        assert ok.all(), worst
+    tiles = (N + 127) // 128
+    counters = host(ws)[: tiles * 4 * 4].view(np.int32)
+    assert not counters.any()
+    assert L.lpq_read_error_word() == 0
+
+
+def test_fp8_static_activation_scale():
+    L = lpq()
+    M, N, K = 64, 256, 512
+    xb = synth.activations(M, K, 5, n_outlier=1, lo=5, hi=6)
+    wb = synth.weights(N, K, 6)
+    s_static = np.float32(0.05)
+    qx = Q.fp8_static(synth.f32_from_bf16_bits(xb), s_static)
+    qw, sw = Q.fp8_per_row(synth.f32_from_bf16_bits(wb))
+    sx = np.array([s_static], np.float32)
+    y, _ = _run(L, qx, sx, qw, sw, M, N, K, static=True)
+    yr, b = G.matmul_ref(C.e4m3fn_decode(qx) * float(s_static), Q.fp8_dequant(qw, sw[:, None]))
+    ok, worst = G.check(bf16_to_f64(y), yr, b)
+    assert ok.all(), worst
+
+
+def test_fp8_gemm_hand_built_codes():
+    """One-hot and max codes: each output is a single product 448 * 448 * s_x * s_w,
+    or a K-long sum of max codes; negative codes and zero rows included."""
+    L = lpq()
+    M, N, K = 130, 144, 256
+    qx = np.zeros((M, K), np.uint8)
+    qw = np.zeros((N, K), np.uint8)
+    for m in range(M):
+        qx[m, (7 * m) % K] = 0x7E if m % 2 else 0xFE
+    for n in range(N):
+        qw[n, (7 * n) % K] = 0x7E
+    qw[5, :] = 0x7E                       # a row of max codes
+    qx[129, :] = 0x01                     # smallest subnormal codes
+    sx = np.linspace(0.5, 2.0, M).astype(np.float32)
+    sw = np.linspace(1.0, 3.0, N).astype(np.float32) / 448
+    y, _ = _run(L, qx, sx, qw, sw, M, N, K)
+    yr, b = _ref(qx, sx, qw, sw)
+    ok, worst = G.check(bf16_to_f64(y), yr, b)
+    assert ok.all(), worst
+    # a one-hot pair that meets gives exactly +-448*448*sx*sw (up to the bf16 rounding)
+    m = 3
+    n = 3
+    assert abs(bf16_to_f64(y)[m, n] - 448.0 * 448.0 * sx[m] * sw[n]) <= C.bf16_ulp(yr[m, n])
+
+
+def test_fp8_end_to_end_quantize_then_gemm():
+    L = lpq()
+    w = synth.configs.TINY_FP8
+    M, (K, N) = 16, (256, 256)
+    xb = synth.configs.make_x(w, M, K)
+    wb = synth.configs.make_w(w, N, K)
+    qx, sx = L.quantize_act_fp8(dev_bf16(xb), L.GRAN_ROW)
+    qw, sw = L.quantize_weight_fp8(dev_bf16(wb), L.GRAN_ROW)
+    Y = L.gemm_scaled(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, qx, qw, sx, sw, M=M, N=N, K=K)
+    torch.cuda.synchronize()
+    qxo, sxo = Q.fp8_per_row(synth.f32_from_bf16_bits(xb))
+    qwo, swo = Q.fp8_per_row(synth.f32_from_bf16_bits(wb))
+    yr, b = _ref(qxo, sxo, qwo, swo)
+    ok, worst = G.check(bf16_to_f64(host(Y)), yr, b)
+    assert ok.all(), worst

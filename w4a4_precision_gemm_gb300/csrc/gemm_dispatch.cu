@@ -1,0 +1,85 @@
+// gemm_dispatch.cu - validation and dispatch of lpq_gemm_scaled.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/lpq.h"
+#include "gemm_fp8.h"
+#include "internal.h"
+
+using namespace lpq;
+
+namespace {
+
+bool is_fp8_rowscale(const lpq_gemm_desc* d) {
+  return d->fmt == LPQ_FMT_FP8 && (d->a_gran == LPQ_GRAN_ROW || d->a_gran == LPQ_GRAN_TENSOR_STATIC) &&
+         d->b_gran == LPQ_GRAN_ROW;
+}
+
+lpq_status validate_common(const lpq_gemm_desc* d, int64_t kmult, int64_t ld_mult) {
+  LPQ_CHECK_NULL(d);
+  LPQ_CHECK_NULL(d->A);
+  LPQ_CHECK_NULL(d->B);
+  LPQ_CHECK_NULL(d->Y);
+  if (d->M <= 0 || d->N <= 0 || d->K <= 0 || d->K % kmult != 0) return LPQ_ERR_SHAPE;
+  if (d->M > 0x7FFFFFFFLL || d->N > 0x7FFFFFFFLL || d->K > 0x7FFFFFFFLL) return LPQ_ERR_SHAPE;
+  if (d->lda < d->K || d->ldb < d->K || d->ldy < d->N) return LPQ_ERR_SHAPE;
+  if (d->lda % ld_mult != 0 || d->ldb % ld_mult != 0 || d->ldy % 8 != 0) return LPQ_ERR_ALIGN;
+  LPQ_CHECK_ALIGN(d->A);
+  LPQ_CHECK_ALIGN(d->B);
+  LPQ_CHECK_ALIGN(d->Y);
+  if (d->workspace && !aligned16(d->workspace)) return LPQ_ERR_ALIGN;
+  return LPQ_OK;
+}
+
+lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st) {
+  lpq_status s = validate_common(d, 16, 16);
+  if (s != LPQ_OK) return s;
+  LPQ_CHECK_NULL(d->sa);
+  LPQ_CHECK_NULL(d->sb);
+  const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, d->workspace != nullptr, d->workspace_bytes);
+  // operand A of the tensor core: X (normal) or W (swap-AB)
+  const void* opA = pl.transposed ? d->B : d->A;
+  const void* opB = pl.transposed ? d->A : d->B;
+  const int64_t ldA = pl.transposed ? d->ldb : d->lda;
+  const int64_t ldB = pl.transposed ? d->lda : d->ldb;
+  CUtensorMap tmA, tmB;
+  if ((s = make_tmap_u8(&tmA, opA, pl.I, d->K, ldA, 128, 128, true)) != LPQ_OK) return s;
+  if ((s = make_tmap_u8(&tmB, opB, pl.J, d->K, ldB, 128, pl.bn, true)) != LPQ_OK) return s;
+  GemmParams p{};
+  p.K = static_cast<int>(d->K);
+  p.sx = static_cast<const float*>(d->sa);
+  p.sx_stride = (d->a_gran == LPQ_GRAN_TENSOR_STATIC) ? 0 : 1;
+  p.sw = static_cast<const float*>(d->sb);
+  p.sw_stride = 1;
+  p.Y = d->Y;
+  p.ldy = d->ldy;
+  p.err = error_word_ptr();
+  return launch_fp8_rowscale(pl, tmA, tmB, p, d->workspace, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
+  if (!d || d->M <= 0 || d->N <= 0 || d->K <= 0) return 0;
+  if (is_fp8_rowscale(d)) {
+    const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX);
+    return fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
+  }
+  return 0;
+}
+
+lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream) {
+  LPQ_CHECK_NULL(d);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d->workspace && d->workspace_bytes < lpq_gemm_workspace_bytes(d)) {
+    // a smaller workspace still works (fewer or no splits); nothing to reject
+  }
+  if (is_fp8_rowscale(d)) return gemm_fp8_rowscale(d, st);
+  return LPQ_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// gemm_fp8.cu - FP8 E4M3 x E4M3 GEMM on the 5th-generation tensor cores with
+// per-row scales applied in the epilogue:
+//   Y = diag(s_X) (X_q W_q^T) diag(s_W)     (fp32 accumulation, bf16 out)
+// "FP8 and FP4 inference, SmoothQuant and activation quantization", section
+// "Scale granularity"; "FP8 and INT8 Inference", sections 5 and 6-9 (the
+// epilogue: acc *= s_a x s_b, store bf16).
+//
+// Structure (one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: 128-byte-swizzled A / B tiles into a STAGES-deep
+//               shared-memory ring (mbarrier full/empty pairs);
+//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread),
+//               accumulating a 128 x BN fp32 tile into one of two TMEM
+//               buffers, so the epilogue of tile t overlaps the K loop of t+1;
+//   warps 2-5   epilogue: tcgen05.ld -> scales -> bf16 -> global (or split-K
+//               partials + an in-order reduction by the last split).
+// Every barrier wait is bounded (a timeout sets the device error word and the
+// kernel winds down); no trap, no unbounded spin.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cstdint>
+
+#include "gemm_common.cuh"
+#include "gemm_fp8.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lpq {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
+
+template <int BN>
+struct Fp8Cfg {
+  static constexpr int kStageBytes = (kBM + BN) * kBKBytes;
+  static constexpr int kStages = cmin(12, (200 * 1024) / kStageBytes);
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  // instruction descriptor: D fp32, A/B E4M3, K-major both, N = BN, M = 128
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_rowscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const GemmParams p) {
+  using C = Fp8Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * kBM * kBKBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * BN * kBKBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto tfull = [&](int a) { return smem_u32(bars + 2 * S + a); };
+  auto tempty = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
+  const uint32_t drain = smem_u32(bars + 2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int units = p.i_tiles * p.j_tiles * p.splits;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_a = p.transposed ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = p.transposed ? policy_evict_last() : policy_evict_first();
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, issued_par = 0;   // per-stage: issued at least once / parity of last issue
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x101u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(full(stage), C::kStageBytes);
+          tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+          tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA leaves
+        volatile int no_abort = 0;
+        for (int s = 0; s < S; ++s)
+          if (issued & (1u << s)) mbar_wait(full(s), (issued_par >> s) & 1u, nullptr, 0, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // --------------------------------------------------------------- MMA
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, p.err, 0x102u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(full(stage), phase, p.err, 0x103u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kBM * kBKBytes);
+          const uint32_t b0 = smem_u32(sB + stage * BN * kBKBytes);
+#pragma unroll
+          for (int k = 0; k < kBKBytes / 32; ++k) {
+            const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, 2);
+            mma_f8f6f4(d, ad, bd, C::kIdesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty(stage));
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // wait for every MMA this thread issued before tensor memory is released
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, nullptr, 0, &no_abort);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x104u, abort_flag)) break;
+      tc_fence_after();
+      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (p.splits > 1) splitk_finish<BN>(p, w, quarter, lane);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int BN>
+lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, cudaStream_t st) {
+  using C = Fp8Cfg<BN>;
+  static uint64_t done_mask = 0;
+  lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes,
+                                  &done_mask);
+  if (s != LPQ_OK) return s;
+  gemm_fp8_rowscale_kernel<BN><<<grid, kThreads, C::kSmemBytes, st>>>(tmA, tmB, p);
+  return after_launch();
+}
+
+}  // namespace
+
+// Tile/split choice: swap-AB (weights on the tensor core's M side) when the
+// token count fits one N tile (<= 256), otherwise 128 x 256 tiles.  Split-K
+// is used when the tiles alone leave SMs idle and a workspace is available.
+Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes) {
+  Fp8Plan pl{};
+  pl.transposed = (M <= 256);
+  const int64_t I = pl.transposed ? N : M;
+  const int64_t J = pl.transposed ? M : N;
+  int bn = 256;
+  if (pl.transposed) {
+    bn = 16;
+    while (bn < J) bn *= 2;
+  }
+  pl.bn = bn;
+  pl.I = I;
+  pl.J = J;
+  pl.i_tiles = static_cast<int>((I + kBM - 1) / kBM);
+  pl.j_tiles = static_cast<int>((J + bn - 1) / bn);
+  pl.kblocks = static_cast<int>((K + kBKBytes - 1) / kBKBytes);
+  const int tiles = pl.i_tiles * pl.j_tiles;
+  const int sms = sm_count();
+  pl.splits = 1;
+  if (have_ws_budget && tiles < sms * 4) {
+    // pick the split count (>= 4 K blocks each) with the best wave efficiency
+    double best = static_cast<double>(tiles) / (((tiles + sms - 1) / sms) * static_cast<double>(sms));
+    for (int s = 2; s <= 32; ++s) {
+      const int per = (pl.kblocks + s - 1) / s;
+      if (per < 4) break;
+      const int real = (pl.kblocks + per - 1) / per;
+      const int units = tiles * real;
+      const double eff = static_cast<double>(units) / (((units + sms - 1) / sms) * static_cast<double>(sms));
+      const size_t need = fp8_ws_bytes(tiles, real, bn);
+      if (need > ws_bytes) continue;
+      if (eff > best + 0.02) {
+        best = eff;
+        pl.splits = real;
+      }
+    }
+  }
+  pl.kb_per_split = (pl.kblocks + pl.splits - 1) / pl.splits;
+  pl.splits = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
+  pl.units = tiles * pl.splits;
+  pl.grid = std::min(pl.units, sms);
+  return pl;
+}
+
+size_t fp8_ws_bytes(int tiles, int splits, int bn) {
+  if (splits <= 1) return 0;
+  const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
+  return counters + static_cast<size_t>(tiles) * splits * 128 * bn * sizeof(float);
+}
+
+lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
+                               void* ws, cudaStream_t st) {
+  p.I = static_cast<int>(pl.I);
+  p.J = static_cast<int>(pl.J);
+  p.i_tiles = pl.i_tiles;
+  p.j_tiles = pl.j_tiles;
+  p.kblocks = pl.kblocks;
+  p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split;
+  p.transposed = pl.transposed;
+  if (pl.splits > 1) {
+    const int tiles = pl.i_tiles * pl.j_tiles;
+    const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
+    p.counters = static_cast<int*>(ws);
+    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
+  }
+  switch (pl.bn) {
+    case 16: return launch_bn<16>(tmA, tmB, p, pl.grid, st);
+    case 32: return launch_bn<32>(tmA, tmB, p, pl.grid, st);
+    case 64: return launch_bn<64>(tmA, tmB, p, pl.grid, st);
+    case 128: return launch_bn<128>(tmA, tmB, p, pl.grid, st);
+    case 256: return launch_bn<256>(tmA, tmB, p, pl.grid, st);
+    default: return LPQ_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace lpq

@@ -1,0 +1,36 @@
+// gemm_fp8.h - host-side planning and launch of the tcgen05 GEMM kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/lpq.h"
+#include "gemm_common.cuh"
+
+namespace lpq {
+
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// Tiling of one FP8 (or FP4) GEMM call.
+struct Fp8Plan {
+  int transposed;     // swap-AB: weights on the tensor core's M side
+  int bn;             // N tile of the tensor core
+  int64_t I, J;       // rows of the A / B operands
+  int i_tiles, j_tiles, kblocks, splits, kb_per_split, units, grid;
+};
+
+Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes);
+size_t fp8_ws_bytes(int tiles, int splits, int bn);
+lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
+                               void* ws, cudaStream_t st);
+
+// Encode a 2-D tensor map over a row-major byte matrix [rows, row_bytes] with
+// row stride ld_bytes, box = box_bytes x box_rows, 128-byte swizzle.
+lpq_status make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int64_t ld_bytes,
+                        int box_bytes, int box_rows, bool swizzle128);
+
+// Set the dynamic shared memory limit of a kernel once per device.
+lpq_status ensure_smem_attr(const void* func, int bytes, uint64_t* done_mask);
+
+}  // namespace lpq
