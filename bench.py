@@ -1,0 +1,432 @@
+"""Benchmark of the quantized-linear hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the hot path over one batch of synthetic input:
+for every token count M and projection (K, N) of the workload, the dynamic
+activation quantizer and the scaled GEMM (weights are quantized once, at load
+time, before timing).  The default workload is Llama-8B-shaped FP8 W8A8
+decode: M in {1, 16, 64, 256} x (K, N) in {(4096, 6144), (4096, 4096),
+(4096, 28672), (14336, 4096)}; every weight copy streamed in a step is
+distinct (no weight byte is read twice per step, 872 MB per step > L2).
+
+Prints one JSON line (rank 0).  `value` is the whole step's GEMM TFLOP/s with
+inputs resident in HBM; `e2e` is the same metric through the C ABI with the
+activations copied from pinned host memory and Y copied back inside the timed
+region; `roofline` is the dominant kernel's achieved HBM GB/s (or tensor
+TFLOP/s) against the measured peak; `cpu_baseline` is the CPU oracle timed on
+a bounded sample of the same workload.  `--impl reference` times that oracle
+as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import configs as CFG  # noqa: E402
+
+
+# ------------------------------------------------------------------ peaks --
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# nominal dense ratios to bf16 (2.25 PF): FP8 4.5 -> 2x, FP4 13.5 -> 6x
+NOMINAL_RATIO = {"fp8": 2.0, "fp4": 6.0, "bf16": 1.0}
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- workloads --
+class Workload:
+    """Holds device buffers and the list of launches of one step."""
+
+    def __init__(self, name, L, torch, rank=0):
+        self.name = name
+        self.L = L
+        self.torch = torch
+        self.rank = rank
+        self.calls = []       # list of dicts: kind, fn (launch), flops, bytes
+
+    def dev_bf16(self, bits):
+        t = self.torch
+        return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).cuda()
+
+
+def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
+    """FP8 W8A8 decode: per-token act quant + swap-AB/split-K FP8 GEMM."""
+    W = Workload(wl.name, L, torch)
+    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "act": "fp8 e4m3 per-token dynamic", "weight": "fp8 e4m3 per-channel static",
+                "l2": "inputs larger than L2: 872 MB of distinct FP8 weights streamed per step"}
+    W.dominant = "gemm_fp8"
+    W.dominant_bound = "hbm"
+    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    for mi, M in enumerate(wl.Ms):
+        for si, (K, N) in enumerate(wl.KNs):
+            wb = CFG.make_w(wl, N, K, salt=si)              # same weights, one fp8 copy per M
+            Wd = W.dev_bf16(wb)
+            Wq, sw = L.quantize_weight_fp8(Wd, L.GRAN_ROW)
+            del Wd
+            xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
+            Xd = W.dev_bf16(xb)
+            Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            sx = torch.empty((M,), dtype=torch.float32, device="cuda")
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
+            desc = L.make_desc(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws)
+            W.keep = getattr(W, "keep", []) + [Wq, sw, ws]
+            W.calls.append(dict(kind="quant_fp8_row", M=M, K=K, N=N,
+                                fn=(lambda Xd=Xd, Xq=Xq, sx=sx: L.lpq_quantize_act_fp8(Xd, L.GRAN_ROW, Xq, sx)),
+                                bytes=M * K * 2 + M * K + 4 * M, flops=0))
+            W.calls.append(dict(kind="gemm_fp8", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
+                                bytes=N * K + 4 * N + M * K + 4 * M + 2 * M * N, flops=2 * M * N * K))
+            W.dev_in.append(Xd)
+            W.dev_out.append(Y)
+            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
+            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+    return W
+
+
+def build_fp4(L, torch, wl):
+    nv = wl.fmt == "nvfp4"
+    W = Workload(wl.name, L, torch)
+    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "format": wl.fmt, "l2": "inputs larger than L2 for M=8192; M=512 weights 37-117 MB"}
+    W.dominant = "gemm_fp4"
+    W.dominant_bound = "tensor"
+    W.dominant_dtype = "fp4"
+    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    F = L.FMT_NVFP4 if nv else L.FMT_MXFP4
+    for mi, M in enumerate(wl.Ms):
+        for si, (K, N) in enumerate(wl.KNs):
+            Wd = W.dev_bf16(CFG.make_w(wl, N, K, salt=si))
+            if nv:
+                Wq, sfw, gsw = L.quantize_nvfp4(Wd)
+            else:
+                (Wq, sfw), gsw = L.quantize_mxfp4(Wd), None
+            del Wd
+            xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
+            Xd = W.dev_bf16(xb)
+            Xq = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+            sfx = torch.empty((L.lpq_sf_bytes(F, M, K),), dtype=torch.uint8, device="cuda")
+            gsx = torch.empty((2,), dtype=torch.float32, device="cuda")
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            ws = L.workspace_for(F, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
+            desc = L.make_desc(F, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sfx, sfw, Y, M=M, N=N, K=K,
+                               ga=gsx[1:] if nv else None, gb=gsw[1:] if nv else None, workspace=ws)
+            W.keep = getattr(W, "keep", []) + [Wq, sfw, gsw, ws, gsx]
+            if nv:
+                qfn = (lambda Xd=Xd, Xq=Xq, sfx=sfx, gsx=gsx: L.lpq_quantize_act_nvfp4(Xd, Xq, sfx, gsx))
+            else:
+                qfn = (lambda Xd=Xd, Xq=Xq, sfx=sfx: L.lpq_quantize_act_mxfp4(Xd, Xq, sfx))
+            blk = 16 if nv else 32
+            W.calls.append(dict(kind="quant_" + wl.fmt, M=M, K=K, N=N, fn=qfn,
+                                bytes=M * K * 2 + M * K // 2 + M * K // blk, flops=0))
+            W.calls.append(dict(kind="gemm_fp4", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
+                                bytes=(M + N) * K // 2 + (M + N) * K // blk + 2 * M * N, flops=2 * M * N * K))
+            W.dev_in.append(Xd)
+            W.dev_out.append(Y)
+            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
+            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+    return W
+
+
+BUILDERS = {
+    "decode_fp8": lambda L, t: build_decode_fp8(L, t),
+    "nvfp4": lambda L, t: build_fp4(L, t, CFG.NVFP4_W4A4),
+    "mxfp4": lambda L, t: build_fp4(L, t, CFG.MXFP4_W4A4),
+}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(workload: str, budget_s: float = 15.0):
+    """Time the CPU oracle on a bounded sample of the workload: every (M, K, N)
+    GEMM of the step, restricted to its first `n_rows` output channels, with
+    the activation quantizer on the full X.  Returns (TFLOP/s, description,
+    threads)."""
+    from oracle import quant as Q
+    from oracle import gemm as G
+    wl = {"decode_fp8": CFG.DECODE_FP8, "nvfp4": CFG.NVFP4_W4A4, "mxfp4": CFG.MXFP4_W4A4}[workload]
+    n_rows = 64
+    Ms = [m for m in wl.Ms if m <= 512] or [wl.Ms[0]]
+    flops, t_total, done = 0, 0.0, 0
+    for mi, M in enumerate(Ms):
+        for si, (K, N) in enumerate(wl.KNs):
+            xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
+            wb = CFG.make_w(wl, n_rows, K, salt=si)
+            x = synth.f32_from_bf16_bits(xb)
+            w = synth.f32_from_bf16_bits(wb)
+            if wl.fmt == "fp8":
+                qw, sw = Q.fp8_per_row(w)                       # load time, untimed
+                t0 = time.perf_counter()
+                qx, sx = Q.fp8_per_row(x)
+                G.matmul_ref(Q.fp8_dequant(qx, sx[:, None]), Q.fp8_dequant(qw, sw[:, None]))
+            elif wl.fmt == "nvfp4":
+                qw, sfw, _, gw = Q.nvfp4(w)
+                t0 = time.perf_counter()
+                qx, sfx, _, gx = Q.nvfp4(x)
+                G.matmul_ref(Q.nvfp4_dequant(qx, sfx, gx), Q.nvfp4_dequant(qw, sfw, gw))
+            else:
+                qw, sfw = Q.mxfp4(w)
+                t0 = time.perf_counter()
+                qx, sfx = Q.mxfp4(x)
+                G.matmul_ref(Q.mxfp4_dequant(qx, sfx), Q.mxfp4_dequant(qw, sfw))
+            t_total += time.perf_counter() - t0
+            flops += 2 * M * n_rows * K
+            done += 1
+            if t_total > budget_s:
+                break
+        if t_total > budget_s:
+            break
+    desc = (f"{done} GEMMs of the step (M<=512) restricted to their first {n_rows} output channels, "
+            f"activation quantizer on the full X; weights quantized untimed")
+    threads = os.cpu_count()
+    return flops / t_total / 1e12, desc, threads
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    vals = []
+    desc, threads = "", os.cpu_count()
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, budget_s=2.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, desc, threads = oracle_sample(args.workload, budget_s=max(2.0, 60.0 / max(1, args.steps)))
+        vals.append(v)
+    el = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "scaled-GEMM TFLOP/s & % of GB300 FP8/FP4 peak; quantizer GB/s & % of HBM"
+
+
+# ------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_fp8", choices=sorted(BUILDERS))
+    ap.add_argument("--impl", default="lpq", choices=["lpq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from w4a4_precision_gemm_gb300 import build as B
+    B.build()
+    from w4a4_precision_gemm_gb300 import lpq as L
+
+    W = BUILDERS[args.workload](L, torch)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        for i, c in enumerate(W.calls):
+            if events is not None:
+                events[i][0].record(stream)
+            c["fn"]()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, per-launch events on the launching stream
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in W.calls]
+           for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    L.lpq_reset_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = L.lpq_launch_count()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if dist:
+        tt = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+
+    flops_step = sum(c["flops"] for c in W.calls)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    # per-kernel statistics from the in-region events
+    kinds = {}
+    for s in range(args.steps):
+        for i, c in enumerate(W.calls):
+            ms = evs[s][i][0].elapsed_time(evs[s][i][1])
+            k = kinds.setdefault(c["kind"], {"launch_ms": 0.0, "launches": 0, "bytes": 0, "flops": 0})
+            k["launch_ms"] += ms
+            k["launches"] += 1
+            k["bytes"] += c["bytes"]
+            k["flops"] += c["flops"]
+    peaks = load_peaks()
+    kern = {}
+    for name, k in kinds.items():
+        kern[name] = {"launches_per_step": k["launches"] // args.steps,
+                      "avg_us": 1000 * k["launch_ms"] / k["launches"],
+                      "GB/s": k["bytes"] / (k["launch_ms"] * 1e-3) / 1e9,
+                      "TFLOP/s": k["flops"] / (k["launch_ms"] * 1e-3) / 1e12 if k["flops"] else 0.0,
+                      "share": k["launch_ms"] / sum(v["launch_ms"] for v in kinds.values())}
+    dom = kinds[W.dominant]
+    if W.dominant_bound == "hbm":
+        achieved = dom["bytes"] / (dom["launch_ms"] * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = dom["flops"] / (dom["launch_ms"] * 1e-3) / 1e12
+        ratio = NOMINAL_RATIO[getattr(W, "dominant_dtype", "fp8")]
+        peak, unit = peaks["bf16_tflops"] * ratio, "TFLOP/s"
+    roofline = {"bound": W.dominant_bound, "kernel": W.dominant, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak,
+                "peak_src": f"{peaks['src']} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops x nominal ratio'})",
+                "traffic": None,
+                "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"]}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    h2d = sum(t.numel() * t.element_size() for t in W.host_in)
+    d2h = sum(t.numel() * t.element_size() for t in W.host_out)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    e_s.record(stream)
+    for _ in range(n_e2e):
+        for h, d in zip(W.host_in, W.dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(W.host_out, W.dev_out):
+            h.copy_(d, non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e) / n_e2e
+    e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, threads = oracle_sample(args.workload)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": {"decode_fp8": "fp8-e4m3 (fp32 accum)",
+                                               "nvfp4": "nvfp4-e2m1 (fp32 accum)",
+                                               "mxfp4": "mxfp4-e2m1 (fp32 accum)"}[args.workload],
+                "data": "synthetic (seeded, pages' shapes and outlier mix)",
+                "config": dict(W.config, parallelism=f"replicas x{world}"),
+                "roofline": roofline, "kernels": kern, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -106,3 +106,5 @@ def random_f32_bits(n: int, seed: int) -> np.ndarray:
     u = _rng(seed).integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
     f = u.view(np.float32)
     return f[np.isfinite(f)]
+
+from . import configs  # noqa: E402  (workload table; imports this module lazily)

@@ -59,6 +59,36 @@ lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st) {
   return launch_fp8_rowscale(pl, tmA, tmB, p, d->workspace, st);
 }
 
+bool is_fp4(const lpq_gemm_desc* d) { return d->fmt == LPQ_FMT_NVFP4 || d->fmt == LPQ_FMT_MXFP4; }
+
+lpq_status gemm_fp4(const lpq_gemm_desc* d, cudaStream_t st) {
+  // element strides; two E2M1 codes per byte, byte strides a multiple of 16
+  lpq_status s = validate_common(d, 32, 32);
+  if (s != LPQ_OK) return s;
+  const bool nv = d->fmt == LPQ_FMT_NVFP4;
+  LPQ_CHECK_NULL(d->sa);
+  LPQ_CHECK_NULL(d->sb);
+  LPQ_CHECK_ALIGN(d->sa);
+  LPQ_CHECK_ALIGN(d->sb);
+  if (nv) {
+    LPQ_CHECK_NULL(d->ga);
+    LPQ_CHECK_NULL(d->gb);
+  }
+  const Fp8Plan pl = plan_fp4(d->M, d->N, d->K, d->workspace != nullptr, d->workspace_bytes);
+  CUtensorMap tmA, tmB;
+  if ((s = make_tmap_u8(&tmA, d->A, d->M, d->K / 2, d->lda / 2, 128, 128, true)) != LPQ_OK) return s;
+  if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K / 2, d->ldb / 2, 128, pl.bn, true)) != LPQ_OK) return s;
+  GemmParams p{};
+  p.K = static_cast<int>(d->K);
+  p.gx = nv ? d->ga : nullptr;
+  p.gw = nv ? d->gb : nullptr;
+  p.Y = d->Y;
+  p.ldy = d->ldy;
+  p.err = error_word_ptr();
+  return launch_fp4(nv, pl, tmA, tmB, static_cast<const uint8_t*>(d->sa), static_cast<const uint8_t*>(d->sb), d->K, p,
+                    d->workspace, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -67,6 +97,10 @@ size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
   if (!d || d->M <= 0 || d->N <= 0 || d->K <= 0) return 0;
   if (is_fp8_rowscale(d)) {
     const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX);
+    return fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
+  }
+  if (is_fp4(d)) {
+    const Fp8Plan pl = plan_fp4(d->M, d->N, d->K, true, SIZE_MAX);
     return fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
   }
   return 0;
@@ -79,6 +113,7 @@ lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream) {
     // a smaller workspace still works (fewer or no splits); nothing to reject
   }
   if (is_fp8_rowscale(d)) return gemm_fp8_rowscale(d, st);
+  if (is_fp4(d)) return gemm_fp4(d, st);
   return LPQ_ERR_UNSUPPORTED;
 }
 

@@ -1,0 +1,299 @@
+// gemm_fp4.cu - W4A4 GEMM on the block-scaled FP4 tensor-core path:
+//   NVFP4: E2M1 x E2M1, one E4M3 scale per 16 elements (scale_vec::4X),
+//          epilogue y = acc * g_x * g_w (the fp32 tensor scales);
+//   MXFP4: E2M1 x E2M1, one E8M0 scale per 32 elements (scale_vec::2X).
+// "FP8 and FP4 inference, SmoothQuant and activation quantization", sections
+// "The bottleneck" (FP4 doubles the rate again over FP8), "Scale granularity"
+// and "Implementation sketch" (nvfp4); "Low-bit LLM Weights and Activations",
+// section 2.4.
+//
+// Same warp roles as the FP8 kernel.  Per pipeline stage the producer loads a
+// 128 x 256 (A) and BN x 256 (B) tile of packed nibbles (one 128-byte
+// swizzled row each) plus the matching scale-factor tiles (512-byte blocks of
+// 128 rows x 4 scales, the layout the quantizers write) with bulk copies.  The
+// MMA thread moves the scales into a per-stage tensor-memory slot with
+// tcgen05.cp (32 lanes x 16 bytes, replicated to the four lane quarters) and
+// issues four K=64 block-scaled MMAs.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cstdint>
+
+#include "gemm_common.cuh"
+#include "gemm_fp8.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lpq {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;        // 256 packed E2M1 elements per row per stage
+constexpr int kKPerStage = 256;
+constexpr int kAtom = 512;           // 128 rows x 4 scale bytes
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int BN, bool NV>
+struct Fp4Cfg {
+  static constexpr int kBlk = NV ? 16 : 32;                    // elements per scale
+  static constexpr int kAtomsPerStage = kKPerStage / kBlk / 4;  // NV 4, MX 2 (per 128 rows)
+  static constexpr int kBGroups = BN / 128;                     // 128-row groups of B (1 or 2)
+  static constexpr int kSfaBytes = kAtomsPerStage * kAtom;
+  static constexpr int kSfbBytes = kBGroups * kAtomsPerStage * kAtom;
+  static constexpr int kStageBytes = (kBM + BN) * kBKBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStages = cmin(8, (200 * 1024) / kStageBytes);
+  // tensor-memory columns: 2 accumulators + per-stage scale slots (4 columns per atom)
+  static constexpr int kSfaCols = kAtomsPerStage * 4;
+  static constexpr int kSfbCols = kBGroups * kAtomsPerStage * 4;
+  static constexpr int kSfCols = kStages * (kSfaCols + kSfbCols);
+  static constexpr int kNeedCols = 2 * BN + kSfCols;
+  static constexpr int kTmemCols = kNeedCols <= 32 ? 32 : kNeedCols <= 64 ? 64 : kNeedCols <= 128 ? 128
+                                   : kNeedCols <= 256 ? 256 : 512;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  // block-scaled instruction descriptor: E2M1 x E2M1 (1), K-major, N, M = 128,
+  // scale type UE4M3 (0, NVFP4) or UE8M0 (1, MXFP4); scale-data ids set per MMA
+  static constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     ((NV ? 0u : 1u) << 23) | (static_cast<uint32_t>(kBM >> 4) << 24);
+};
+static_assert(Fp4Cfg<128, true>::kNeedCols <= 512, "tensor memory budget");
+
+template <int BN, bool NV>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int64_t sf_kb4,
+                    const GemmParams p) {
+  using C = Fp4Cfg<BN, NV>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * kBM * kBKBytes;
+  uint8_t* sSFA = sB + S * BN * kBKBytes;
+  uint8_t* sSFB = sSFA + S * C::kSfaBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + S * C::kSfbBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto tfull = [&](int a) { return smem_u32(bars + 2 * S + a); };
+  auto tempty = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
+  const uint32_t drain = smem_u32(bars + 2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = p.i_tiles * p.j_tiles * p.splits;
+  // MMA k-steps (64 elements) in the last, possibly partial, stage
+  const int ksteps_total = (p.K + 63) / 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_a = p.transposed ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = p.transposed ? policy_evict_last() : policy_evict_first();
+      uint32_t stage = 0, phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x201u, abort_flag)) { ok = false; break; }
+          // scale atoms of this stage that exist (a partial last stage has fewer)
+          const int ksteps = min(4, ksteps_total - kb * 4);
+          const int atoms = NV ? ksteps : (ksteps + 1) / 2;
+          const uint32_t sf_bytes = atoms * kAtom;
+          mbar_arrive_expect_tx(full(stage), (kBM + BN) * kBKBytes + sf_bytes * (1 + C::kBGroups));
+          tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+          tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+          const int64_t atom0 = static_cast<int64_t>(kb) * C::kAtomsPerStage;
+          bulk_g2s(smem_u32(sSFA + stage * C::kSfaBytes), sfa + (w.i_tile * sf_kb4 + atom0) * kAtom, sf_bytes,
+                   full(stage));
+#pragma unroll
+          for (int g = 0; g < C::kBGroups; ++g)
+            bulk_g2s(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes),
+                     sfb + ((w.j_tile * C::kBGroups + g) * sf_kb4 + atom0) * kAtom, sf_bytes, full(stage));
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < S; ++s)
+          if (issued & (1u << s)) mbar_wait(full(s), (issued_par >> s) & 1u, nullptr, 0, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      const uint32_t sf_base = tmem_base + 2 * BN;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (!mbar_wait(tempty(acc), acc_phase ^ 1u, p.err, 0x202u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(full(stage), phase, p.err, 0x203u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const int ksteps = min(4, ksteps_total - kb * 4);
+          const int atoms = NV ? ksteps : (ksteps + 1) / 2;
+          const uint32_t tsfa = sf_base + stage * (C::kSfaCols + C::kSfbCols);
+          const uint32_t tsfb = tsfa + C::kSfaCols;
+          // scales: smem -> tensor memory (4 columns per 512-byte atom)
+          for (int a = 0; a < atoms; ++a) {
+            tc_cp_32x128b_warpx4(tsfa + a * 4, smem_desc(smem_u32(sSFA + stage * C::kSfaBytes + a * kAtom), 16, 128, 0));
+#pragma unroll
+            for (int g = 0; g < C::kBGroups; ++g)
+              tc_cp_32x128b_warpx4(tsfb + (g * C::kAtomsPerStage + a) * 4,
+                                   smem_desc(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes + a * kAtom), 16,
+                                             128, 0));
+          }
+          const uint32_t a0 = smem_u32(sA + stage * kBM * kBKBytes);
+          const uint32_t b0 = smem_u32(sB + stage * BN * kBKBytes);
+          for (int k = 0; k < ksteps; ++k) {
+            const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, 2);
+            const uint32_t acc_in = (kb > w.kb0 || k > 0) ? 1u : 0u;
+            if constexpr (NV) {
+              mma_nvf4(d, ad, bd, C::kIdesc, tsfa + k * 4, tsfb + k * 4, acc_in);
+            } else {
+              const uint32_t id = static_cast<uint32_t>((k & 1) * 2);
+              const uint32_t idesc = C::kIdesc | (id << 4) | (id << 29);
+              mma_mxf4(d, ad, bd, idesc, tsfa + (k >> 1) * 4, tsfb + (k >> 1) * 4, acc_in);
+            }
+          }
+          tc_commit(empty(stage));
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, nullptr, 0, &no_abort);
+    }
+  } else {
+    const int quarter = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
+      tc_fence_after();
+      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (p.splits > 1) splitk_finish<BN>(p, w, quarter, lane);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int BN, bool NV>
+lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa, const uint8_t* sfb,
+                        int64_t kb4, const GemmParams& p, int grid, cudaStream_t st) {
+  using C = Fp4Cfg<BN, NV>;
+  static uint64_t done_mask = 0;
+  lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp4_kernel<BN, NV>), C::kSmemBytes, &done_mask);
+  if (s != LPQ_OK) return s;
+  gemm_fp4_kernel<BN, NV><<<grid, kThreads, C::kSmemBytes, st>>>(tmA, tmB, sfa, sfb, kb4, p);
+  return after_launch();
+}
+
+}  // namespace
+
+// FP4 plan: always 128 x 128 tiles on the natural operands (no swap; the
+// scale layouts of A and B are the same 128-row tiles).  Split-K when the
+// tiles leave SMs idle and a workspace is given.
+Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes) {
+  Fp8Plan pl{};
+  pl.transposed = 0;
+  pl.bn = 128;
+  pl.I = M;
+  pl.J = N;
+  pl.i_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  pl.j_tiles = static_cast<int>((N + pl.bn - 1) / pl.bn);
+  pl.kblocks = static_cast<int>((K + kKPerStage - 1) / kKPerStage);
+  const int tiles = pl.i_tiles * pl.j_tiles;
+  const int sms = sm_count();
+  pl.splits = 1;
+  if (have_ws && tiles < sms * 4) {
+    double best = static_cast<double>(tiles) / (((tiles + sms - 1) / sms) * static_cast<double>(sms));
+    for (int s = 2; s <= 32; ++s) {
+      const int per = (pl.kblocks + s - 1) / s;
+      if (per < 4) break;
+      const int real = (pl.kblocks + per - 1) / per;
+      const int units = tiles * real;
+      const double eff = static_cast<double>(units) / (((units + sms - 1) / sms) * static_cast<double>(sms));
+      if (fp8_ws_bytes(tiles, real, pl.bn) > ws_bytes) continue;
+      if (eff > best + 0.02) {
+        best = eff;
+        pl.splits = real;
+      }
+    }
+  }
+  pl.kb_per_split = (pl.kblocks + pl.splits - 1) / pl.splits;
+  pl.splits = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
+  pl.units = tiles * pl.splits;
+  pl.grid = std::min(pl.units, sms);
+  return pl;
+}
+
+lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa,
+                      const uint8_t* sfb, int64_t K, GemmParams p, void* ws, cudaStream_t st) {
+  p.I = static_cast<int>(pl.I);
+  p.J = static_cast<int>(pl.J);
+  p.i_tiles = pl.i_tiles;
+  p.j_tiles = pl.j_tiles;
+  p.kblocks = pl.kblocks;
+  p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split;
+  p.transposed = 0;
+  if (pl.splits > 1) {
+    const int tiles = pl.i_tiles * pl.j_tiles;
+    const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
+    p.counters = static_cast<int*>(ws);
+    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
+  }
+  const int64_t kb4 = (K / (nv ? 16 : 32) + 3) / 4;
+  if (nv) return launch_fp4_t<128, true>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
+  return launch_fp4_t<128, false>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
+}
+
+}  // namespace lpq

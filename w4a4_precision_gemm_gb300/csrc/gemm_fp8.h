@@ -25,6 +25,10 @@ size_t fp8_ws_bytes(int tiles, int splits, int bn);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st);
 
+Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes);
+lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa,
+                      const uint8_t* sfb, int64_t K, GemmParams p, void* ws, cudaStream_t st);
+
 // Encode a 2-D tensor map over a row-major byte matrix [rows, row_bytes] with
 // row stride ld_bytes, box = box_bytes x box_rows, 128-byte swizzle.
 lpq_status make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int64_t ld_bytes,
