@@ -59,6 +59,22 @@ lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st) {
   return launch_fp8_rowscale(pl, tmA, tmB, p, d->workspace, st);
 }
 
+bool is_fp8_block(const lpq_gemm_desc* d) {
+  return d->fmt == LPQ_FMT_FP8 && d->a_gran == LPQ_GRAN_BLOCK_1x128 && d->b_gran == LPQ_GRAN_BLOCK_128x128;
+}
+
+lpq_status gemm_fp8_block(const lpq_gemm_desc* d, cudaStream_t st) {
+  lpq_status s = validate_common(d, 128, 16);
+  if (s != LPQ_OK) return s;
+  LPQ_CHECK_NULL(d->sa);
+  LPQ_CHECK_NULL(d->sb);
+  CUtensorMap tmA, tmB;
+  if ((s = make_tmap_u8(&tmA, d->A, d->M, d->K, d->lda, 128, 128, true)) != LPQ_OK) return s;
+  if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K, d->ldb, 128, 128, true)) != LPQ_OK) return s;
+  return launch_fp8_block(tmA, tmB, d->M, d->N, d->K, static_cast<const float*>(d->sa),
+                          static_cast<const float*>(d->sb), d->Y, d->ldy, st);
+}
+
 bool is_fp4(const lpq_gemm_desc* d) { return d->fmt == LPQ_FMT_NVFP4 || d->fmt == LPQ_FMT_MXFP4; }
 
 lpq_status gemm_fp4(const lpq_gemm_desc* d, cudaStream_t st) {
@@ -113,6 +129,7 @@ lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream) {
     // a smaller workspace still works (fewer or no splits); nothing to reject
   }
   if (is_fp8_rowscale(d)) return gemm_fp8_rowscale(d, st);
+  if (is_fp8_block(d)) return gemm_fp8_block(d, st);
   if (is_fp4(d)) return gemm_fp4(d, st);
   return LPQ_ERR_UNSUPPORTED;
 }

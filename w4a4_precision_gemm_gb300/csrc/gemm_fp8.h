@@ -25,6 +25,9 @@ size_t fp8_ws_bytes(int tiles, int splits, int bn);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st);
 
+lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
+                            const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
+
 Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes);
 lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa,
                       const uint8_t* sfb, int64_t K, GemmParams p, void* ws, cudaStream_t st);
