@@ -289,6 +289,7 @@ def main():
     ap.add_argument("--workload", default="decode_fp8", choices=sorted(BUILDERS))
     ap.add_argument("--impl", default="lpq", choices=["lpq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="keep only these M:N pairs, e.g. 1:28672,16:4096 (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -309,6 +310,15 @@ def main():
     from w4a4_precision_gemm_gb300 import lpq as L
 
     W = BUILDERS[args.workload](L, torch)
+    if args.only:
+        keep = {tuple(int(v) for v in p.split(":")) for p in args.only.split(",")}
+        idx = [i for i in range(0, len(W.calls), 2) if (W.calls[i]["M"], W.calls[i]["N"]) in keep]
+        W.calls = [W.calls[j] for i in idx for j in (i, i + 1)]
+        W.dev_in = [W.dev_in[i // 2] for i in idx]
+        W.dev_out = [W.dev_out[i // 2] for i in idx]
+        W.host_in = [W.host_in[i // 2] for i in idx]
+        W.host_out = [W.host_out[i // 2] for i in idx]
+        W.config["only"] = args.only
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -360,11 +370,12 @@ def main():
     for s in range(args.steps):
         for i, c in enumerate(W.calls):
             ms = evs[s][i][0].elapsed_time(evs[s][i][1])
-            k = kinds.setdefault(c["kind"], {"launch_ms": 0.0, "launches": 0, "bytes": 0, "flops": 0})
-            k["launch_ms"] += ms
-            k["launches"] += 1
-            k["bytes"] += c["bytes"]
-            k["flops"] += c["flops"]
+            for key in (c["kind"], f'{c["kind"]}[M={c["M"]},K={c["K"]},N={c["N"]}]'):
+                k = kinds.setdefault(key, {"launch_ms": 0.0, "launches": 0, "bytes": 0, "flops": 0})
+                k["launch_ms"] += ms
+                k["launches"] += 1
+                k["bytes"] += c["bytes"]
+                k["flops"] += c["flops"]
     peaks = load_peaks()
     kern = {}
     for name, k in kinds.items():
@@ -372,7 +383,7 @@ def main():
                       "avg_us": 1000 * k["launch_ms"] / k["launches"],
                       "GB/s": k["bytes"] / (k["launch_ms"] * 1e-3) / 1e9,
                       "TFLOP/s": k["flops"] / (k["launch_ms"] * 1e-3) / 1e12 if k["flops"] else 0.0,
-                      "share": k["launch_ms"] / sum(v["launch_ms"] for v in kinds.values())}
+                      "share": k["launch_ms"] / sum(v["launch_ms"] for n, v in kinds.items() if "[" not in n)}
     dom = kinds[W.dominant]
     if W.dominant_bound == "hbm":
         achieved = dom["bytes"] / (dom["launch_ms"] * 1e-3) / 1e9
