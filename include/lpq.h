@@ -194,6 +194,29 @@ typedef struct {
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d);
 lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream);
 
+/* ------------------------------------------- GEMM without a workspace -- */
+/* The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: a plugin inside a serving runtime that owns
+ * all device memory through its own pool and hands over only the operation's
+ * tensors, or a latency-critical path where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable and no workspace was set aside.
+ *
+ * Same operation and arguments as lpq_gemm_scaled for fmt LPQ_FMT_FP8 with
+ * a_gran ROW or TENSOR_STATIC and b_gran ROW (other combinations return
+ * LPQ_ERR_UNSUPPORTED); d->workspace is ignored.  The split-K scratch comes
+ * from one array of LPQ_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits.  A problem whose
+ * split-K scratch would exceed that size returns LPQ_ERR_WORKSPACE and
+ * enqueues nothing; nothing is allocated or freed.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device, done with that device current); make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * previous call's contents: the call clears its tile counters itself, but
+ * calls that may run at the same time on the GPU race on the array; order
+ * them on one stream. */
+#define LPQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
