@@ -38,6 +38,56 @@ import synth  # noqa: E402
 from synth import configs as CFG  # noqa: E402
 
 
+# -------------------------------------------------------- graph timing --
+class GraphEvents:
+    """Timing events that can live inside a CUDA graph: recorded with
+    cudaEventRecordWithFlags(..., cudaEventRecordExternal), so that stream
+    capture turns them into event-record nodes (torch's Event.record inside a
+    capture only orders streams).  Uses the process's CUDA runtime."""
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.rt = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                self.rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.rt is None:
+            raise RuntimeError("CUDA runtime library not found for graph timing events")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+        self.events = []
+
+    def new(self):
+        e = self.ct.c_void_p()
+        if self.rt.cudaEventCreate(self.ct.byref(e)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        self.events.append(e)
+        return e
+
+    def record(self, ev, stream):
+        r = self.rt.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), 1)
+        if r != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed ({r})")
+
+    def elapsed_ms(self, a, b):
+        f = self.ct.c_float()
+        r = self.rt.cudaEventElapsedTime(self.ct.byref(f), a, b)
+        if r != 0:
+            raise RuntimeError(f"cudaEventElapsedTime failed ({r})")
+        return f.value
+
+    def close(self):
+        for e in self.events:
+            self.rt.cudaEventDestroy(e)
+        self.events = []
+
+
 # ------------------------------------------------------------------ peaks --
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -121,7 +171,7 @@ class Workload:
 
 
 def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
-    """FP8 W8A8 decode: per-token act quant + swap-AB/split-K FP8 GEMM."""
+    """FP8 W8A8 decode: per-token act quant + swap-AB / stream-K FP8 GEMM."""
     W = Workload(wl.name, L, torch)
     W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
                 "act": "fp8 e4m3 per-token dynamic", "weight": "fp8 e4m3 per-channel static",
@@ -289,6 +339,7 @@ def main():
     ap.add_argument("--workload", default="decode_fp8", choices=sorted(BUILDERS))
     ap.add_argument("--impl", default="lpq", choices=["lpq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch every call from Python instead of a CUDA graph")
     ap.add_argument("--only", default="", help="keep only these M:N pairs, e.g. 1:28672,16:4096 (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -322,36 +373,64 @@ def main():
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def step(events=None):
-        for i, c in enumerate(W.calls):
-            if events is not None:
-                events[i][0].record(stream)
+    def step():
+        for c in W.calls:
             c["fn"]()
-            if events is not None:
-                events[i][1].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, per-launch events on the launching stream
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in W.calls]
-           for _ in range(args.steps)]
+    # ---- the K timed steps, captured once into a CUDA graph (the library's
+    # calls are plain stream work, so capture records them as kernel nodes);
+    # per-launch timing events are event-record nodes inside the graph
+    GE = GraphEvents()
+    evs = [[(GE.new(), GE.new()) for _ in W.calls] for _ in range(args.steps)]
+    cap = torch.cuda.Stream()
+
+    def timed_steps(on):
+        for s_ in range(args.steps):
+            for i, c in enumerate(W.calls):
+                GE.record(evs[s_][i][0], on)
+                c["fn"]()
+                GE.record(evs[s_][i][1], on)
+
+    graph = None
+    if not args.eager:
+        try:
+            cap.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            L.lpq_reset_launch_count()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    timed_steps(cap)
+            stream.wait_stream(cap)
+            launches = L.lpq_launch_count()   # library kernels in the graph = launches in the timed region
+            graph.replay()                    # one untimed replay of the graph itself
+            torch.cuda.synchronize()
+        except Exception as e:  # capture unavailable: time the same calls eagerly
+            print(f"bench: graph capture failed ({e}); timing eagerly", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    L.lpq_reset_launch_count()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if graph is None:
+        L.lpq_reset_launch_count()
     t_start.record(stream)
-    for s in range(args.steps):
-        step(evs[s])
+    if graph is not None:
+        graph.replay()
+    else:
+        timed_steps(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
-    launches = L.lpq_launch_count()
+    if graph is None:
+        launches = L.lpq_launch_count()
     if dist:
         dist.barrier()
     clocks = clk.stop()
@@ -369,7 +448,7 @@ def main():
     kinds = {}
     for s in range(args.steps):
         for i, c in enumerate(W.calls):
-            ms = evs[s][i][0].elapsed_time(evs[s][i][1])
+            ms = GE.elapsed_ms(evs[s][i][0], evs[s][i][1])
             for key in (c["kind"], f'{c["kind"]}[M={c["M"]},K={c["K"]},N={c["N"]}]'):
                 k = kinds.setdefault(key, {"launch_ms": 0.0, "launches": 0, "bytes": 0, "flops": 0})
                 k["launch_ms"] += ms
@@ -398,23 +477,44 @@ def main():
                 "traffic": None,
                 "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"]}
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    # ---- end to end through the C ABI with host buffers (pinned): every step
+    # copies its activations in and its Y out; the calls are captured in a
+    # graph the way a serving loop replays them
     h2d = sum(t.numel() * t.element_size() for t in W.host_in)
     d2h = sum(t.numel() * t.element_size() for t in W.host_out)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_e2e = max(3, args.steps // 2)
+
+    def e2e_steps():
+        for _ in range(n_e2e):
+            for h, d in zip(W.host_in, W.dev_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(W.host_out, W.dev_out):
+                h.copy_(d, non_blocking=True)
+
+    g2 = None
+    if graph is not None:
+        g2 = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g2, stream=cap):
+                e2e_steps()
+        stream.wait_stream(cap)
+        g2.replay()
+    else:
+        e2e_steps()
     torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_s.record(stream)
-    for _ in range(n_e2e):
-        for h, d in zip(W.host_in, W.dev_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(W.host_out, W.dev_out):
-            h.copy_(d, non_blocking=True)
+    if g2 is not None:
+        g2.replay()
+    else:
+        e2e_steps()
     e_e.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_s.elapsed_time(e_e) / n_e2e
     e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    GE.close()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -432,7 +532,8 @@ def main():
                 "roofline": roofline, "kernels": kern, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
-                "gpu_launches": launches, "clocks": clocks}
+                "gpu_launches": launches, "clocks": clocks,
+                "launch_mode": "cuda-graph replay" if graph is not None else "eager"}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

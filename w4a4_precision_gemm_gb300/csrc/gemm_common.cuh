@@ -1,5 +1,6 @@
 // gemm_common.cuh - pieces shared by the tcgen05 GEMM kernels: work-unit
-// decoding, the scale epilogue and the split-K reduction.
+// decoding (data-parallel tiles or stream-K ranges), the scale epilogue and
+// the in-order combination of stream-K partial tiles.
 //
 // Every GEMM here computes D[i, j] = sum_k A[i, k] B[j, k] for a 128-row tile
 // of the "A" operand (the tensor core's M side) and a BN-row tile of the "B"
@@ -18,32 +19,77 @@ struct GemmParams {
   int I, J, K;                 // rows of A, rows of B, reduction length (elements)
   int i_tiles, j_tiles;        // tiles of 128 rows of A, BN rows of B
   int kblocks;                 // K blocks (one pipeline stage each)
-  int splits, kb_per_split;    // split-K
+  int streamk;                 // 0: whole tiles round-robin; 1: equal K-iteration ranges per CTA
   int transposed;              // 0: Y[i][j], 1: Y[j][i]
   // epilogue scales: y = (acc * s_x) * s_w, s_x / s_w read from the i or j side
   const float* sx; int sx_stride;                // sx_stride 0: one scale for all
   const float* sw; int sw_stride;
   const float* gx; const float* gw;              // optional extra factors (NVFP4 g)
   uint16_t* Y; int64_t ldy;
-  float* ws;                   // split-K partials [tiles * splits][128][BN]
+  float* ws;                   // stream-K partials [grid][2][128][BN]
   int* counters;               // [tiles * 4], zero on entry, zero on exit
   uint32_t* err;
 };
 
-struct Unit {
-  int tile, split, i_tile, j_tile, kb0, kb1;
+// A piece of work for one CTA: K blocks [kb0, kb1) of one output tile.
+// `full` pieces cover the whole K range; the others are stream-K pieces whose
+// partial sums are combined by the last of the tile's contributors.
+struct Seg {
+  int tile, i_tile, j_tile, kb0, kb1;
+  bool full;
+  int g_first, n_contrib, slot;
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
-  Unit w;
-  w.tile = u / p.splits;
-  w.split = u - w.tile * p.splits;
-  w.i_tile = w.tile % p.i_tiles;
-  w.j_tile = w.tile / p.i_tiles;
-  w.kb0 = w.split * p.kb_per_split;
-  w.kb1 = min(p.kblocks, w.kb0 + p.kb_per_split);
-  return w;
-}
+// Iterates the pieces of CTA `g` of `G`.  Data-parallel mode: tiles g, g+G,
+// ...  Stream-K mode: the contiguous range [g T / G, (g+1) T / G) of the
+// T = tiles x kblocks (tile-major) K iterations, cut at tile boundaries.
+struct WorkIter {
+  int64_t it, end;
+  int tile_rr;
+  __device__ __forceinline__ WorkIter(const GemmParams& p, int g, int G) {
+    const int64_t T = static_cast<int64_t>(p.i_tiles) * p.j_tiles * p.kblocks;
+    it = p.streamk ? (static_cast<int64_t>(g) * T) / G : 0;
+    end = p.streamk ? (static_cast<int64_t>(g + 1) * T) / G : 0;
+    tile_rr = g;
+  }
+  // CTA whose range holds iteration x: the largest g with floor(g T / G) <= x
+  __device__ __forceinline__ static int owner(int64_t x, int64_t T, int G) {
+    return static_cast<int>(((x + 1) * G - 1) / T);
+  }
+  __device__ __forceinline__ bool next(const GemmParams& p, int g, int G, Seg& s) {
+    const int tiles = p.i_tiles * p.j_tiles;
+    if (!p.streamk) {
+      if (tile_rr >= tiles) return false;
+      s.tile = tile_rr;
+      tile_rr += G;
+      s.kb0 = 0;
+      s.kb1 = p.kblocks;
+    } else {
+      if (it >= end) return false;
+      s.tile = static_cast<int>(it / p.kblocks);
+      s.kb0 = static_cast<int>(it - static_cast<int64_t>(s.tile) * p.kblocks);
+      const int64_t left = end - it;
+      s.kb1 = static_cast<int>(s.kb0 + left < p.kblocks ? s.kb0 + left : p.kblocks);
+      it += s.kb1 - s.kb0;
+    }
+    s.i_tile = s.tile % p.i_tiles;
+    s.j_tile = s.tile / p.i_tiles;
+    s.full = (s.kb0 == 0 && s.kb1 == p.kblocks);
+    s.g_first = g;
+    s.n_contrib = 1;
+    s.slot = 0;
+    if (!s.full) {
+      const int64_t T = static_cast<int64_t>(tiles) * p.kblocks;
+      const int64_t a = static_cast<int64_t>(s.tile) * p.kblocks;
+      s.g_first = owner(a, T, G);
+      s.n_contrib = owner(a + p.kblocks - 1, T, G) - s.g_first + 1;
+      // the first contributor's piece is the last of its range (slot 1); every
+      // later contributor's piece is the first of its range (slot 0)
+      s.slot = (g == s.g_first) ? 1 : 0;
+    }
+    return true;
+  }
+};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -104,75 +150,58 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j
 }
 
 // Tensor-memory -> registers -> epilogue for one 128 x BN accumulator, by the
-// four epilogue warps (warp q of the CTA reads lanes 32*(q%4) .. +31).
-// Without split-K the result is scaled and stored; with split-K the partial is
-// written to the workspace and the last of the splits of this tile (per
-// 32-row quarter) sums all partials in split order and stores the result.
+// four epilogue warps (warp q of the CTA reads lanes 32*(q%4) .. +31).  A full
+// piece is scaled and stored; a stream-K piece writes its partial sums to its
+// slot of the workspace.
 template <int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Unit& w, uint32_t tmem_acc, int quarter,
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w, uint32_t tmem_acc, int quarter,
                                               int lane) {
   constexpr int CW = (BN < 32) ? BN : 32;
   const int row_in_tile = quarter * 32 + lane;
   const int i = w.i_tile * 128 + row_in_tile;
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
-  if (p.splits == 1) {
-#pragma unroll 1
-    for (int c = 0; c < BN; c += CW) {
-      float v[CW];
-      if constexpr (CW == 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
-      } else {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(taddr + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(r[t]);
-      }
-      epilogue_store<CW>(p, i, w.j_tile * BN + c, v);
-    }
-    return;
-  }
-  // split-K: write this split's partial
-  float* part = p.ws + ((static_cast<int64_t>(w.tile) * p.splits + w.split) * 128 + row_in_tile) * BN;
+  float* part = w.full ? nullptr
+                       : p.ws + ((static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 + row_in_tile) * BN;
 #pragma unroll 1
   for (int c = 0; c < BN; c += CW) {
+    float v[CW];
     if constexpr (CW == 32) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(taddr + c, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int t = 0; t < 32; t += 4)
-        __stcg(reinterpret_cast<float4*>(part + c + t),
-               make_float4(__uint_as_float(r[t]), __uint_as_float(r[t + 1]), __uint_as_float(r[t + 2]),
-                           __uint_as_float(r[t + 3])));
+      for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
     } else {
       uint32_t r[16];
       tmem_ld_32x32b_x16(taddr + c, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int t = 0; t < 16; t += 4)
-        __stcg(reinterpret_cast<float4*>(part + c + t),
-               make_float4(__uint_as_float(r[t]), __uint_as_float(r[t + 1]), __uint_as_float(r[t + 2]),
-                           __uint_as_float(r[t + 3])));
+      for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(r[t]);
+    }
+    if (w.full) {
+      epilogue_store<CW>(p, i, w.j_tile * BN + c, v);
+    } else {
+#pragma unroll
+      for (int t = 0; t < CW; t += 4)
+        __stcg(reinterpret_cast<float4*>(part + c + t), make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
     }
   }
 }
 
-// Second half of the split-K epilogue, run after the accumulator has been
-// handed back to the MMA warp.
+// Second half of a stream-K piece, run after the accumulator has been handed
+// back to the MMA warp: count this quarter-tile in; the last contributor sums
+// every contributor's partial in contributor order (a fixed order, so the
+// result does not depend on which CTA finishes last) and stores the tile.
 template <int BN>
-__device__ __forceinline__ void splitk_finish(const GemmParams& p, const Unit& w, int quarter, int lane) {
-  constexpr int CW = (BN < 32) ? BN : 32;
+__device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w, int quarter, int lane) {
+  constexpr int kSub = 8;          // columns per reduction step
+  constexpr int kBatch = 8;        // contributors whose loads are in flight together
   __threadfence();
   __syncwarp();
   int last = 0;
   if (lane == 0) {
     const int old = atomicAdd(p.counters + w.tile * 4 + quarter, 1);
-    last = (old == p.splits - 1);
+    last = (old == w.n_contrib - 1);
     if (last) p.counters[w.tile * 4 + quarter] = 0;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
@@ -180,21 +209,34 @@ __device__ __forceinline__ void splitk_finish(const GemmParams& p, const Unit& w
   __threadfence();
   const int row_in_tile = quarter * 32 + lane;
   const int i = w.i_tile * 128 + row_in_tile;
-#pragma unroll 1
-  for (int c = 0; c < BN; c += CW) {
-    float v[CW];
+  const int64_t row_off = static_cast<int64_t>(row_in_tile) * BN;
+#pragma unroll 2
+  for (int c = 0; c < BN; c += kSub) {
+    float v[kSub];
 #pragma unroll
-    for (int t = 0; t < CW; ++t) v[t] = 0.0f;
-#pragma unroll 1
-    for (int s = 0; s < p.splits; ++s) {
-      const float* part = p.ws + ((static_cast<int64_t>(w.tile) * p.splits + s) * 128 + row_in_tile) * BN + c;
+    for (int t = 0; t < kSub; ++t) v[t] = 0.0f;
+    for (int s0 = 0; s0 < w.n_contrib; s0 += kBatch) {
+      float4 f[kBatch][2];
 #pragma unroll
-      for (int t = 0; t < CW; t += 4) {
-        const float4 f = __ldcg(reinterpret_cast<const float4*>(part + t));
-        v[t] += f.x; v[t + 1] += f.y; v[t + 2] += f.z; v[t + 3] += f.w;
+      for (int b = 0; b < kBatch; ++b) {
+        if (s0 + b < w.n_contrib) {
+          const int g = w.g_first + s0 + b;
+          const int slot = (s0 + b == 0) ? 1 : 0;
+          const float4* part = reinterpret_cast<const float4*>(
+              p.ws + (static_cast<int64_t>(g) * 2 + slot) * 128 * BN + row_off + c);
+          f[b][0] = __ldcg(part);
+          f[b][1] = __ldcg(part + 1);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (s0 + b < w.n_contrib) {
+          v[0] += f[b][0].x; v[1] += f[b][0].y; v[2] += f[b][0].z; v[3] += f[b][0].w;
+          v[4] += f[b][1].x; v[5] += f[b][1].y; v[6] += f[b][1].z; v[7] += f[b][1].w;
+        }
       }
     }
-    epilogue_store<CW>(p, i, w.j_tile * BN + c, v);
+    epilogue_store<kSub>(p, i, w.j_tile * BN + c, v);
   }
 }
 

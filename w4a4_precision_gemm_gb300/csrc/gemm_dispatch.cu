@@ -75,6 +75,22 @@ lpq_status gemm_fp8_block(const lpq_gemm_desc* d, cudaStream_t st) {
                           static_cast<const float*>(d->sb), d->Y, d->ldy, st);
 }
 
+bool is_int8(const lpq_gemm_desc* d) {
+  return d->fmt == LPQ_FMT_INT8 && d->a_gran == LPQ_GRAN_ROW && d->b_gran == LPQ_GRAN_ROW;
+}
+
+lpq_status gemm_int8(const lpq_gemm_desc* d, cudaStream_t st) {
+  lpq_status s = validate_common(d, 16, 16);
+  if (s != LPQ_OK) return s;
+  LPQ_CHECK_NULL(d->sa);
+  LPQ_CHECK_NULL(d->sb);
+  CUtensorMap tmA, tmB;
+  if ((s = make_tmap_u8(&tmA, d->A, d->M, d->K, d->lda, 128, 128, true)) != LPQ_OK) return s;
+  if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K, d->ldb, 128, 128, true)) != LPQ_OK) return s;
+  return launch_int8(tmA, tmB, d->M, d->N, d->K, static_cast<const float*>(d->sa), static_cast<const float*>(d->sb),
+                     d->Y, d->ldy, st);
+}
+
 bool is_fp4(const lpq_gemm_desc* d) { return d->fmt == LPQ_FMT_NVFP4 || d->fmt == LPQ_FMT_MXFP4; }
 
 lpq_status gemm_fp4(const lpq_gemm_desc* d, cudaStream_t st) {
@@ -112,12 +128,10 @@ extern "C" {
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
   if (!d || d->M <= 0 || d->N <= 0 || d->K <= 0) return 0;
   if (is_fp8_rowscale(d)) {
-    const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX);
-    return fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
+    return plan_ws_bytes(plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX));
   }
   if (is_fp4(d)) {
-    const Fp8Plan pl = plan_fp4(d->M, d->N, d->K, true, SIZE_MAX);
-    return fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
+    return plan_ws_bytes(plan_fp4(d->M, d->N, d->K, true, SIZE_MAX));
   }
   return 0;
 }
@@ -125,11 +139,11 @@ size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
 lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream) {
   LPQ_CHECK_NULL(d);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d->workspace && d->workspace_bytes < lpq_gemm_workspace_bytes(d)) {
-    // a smaller workspace still works (fewer or no splits); nothing to reject
-  }
+  // a workspace smaller than lpq_gemm_workspace_bytes still works: the
+  // planner then falls back to whole tiles
   if (is_fp8_rowscale(d)) return gemm_fp8_rowscale(d, st);
   if (is_fp8_block(d)) return gemm_fp8_block(d, st);
+  if (is_int8(d)) return gemm_int8(d, st);
   if (is_fp4(d)) return gemm_fp4(d, st);
   return LPQ_ERR_UNSUPPORTED;
 }

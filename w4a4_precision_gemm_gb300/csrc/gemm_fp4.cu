@@ -113,7 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int units = p.i_tiles * p.j_tiles * p.splits;
   // MMA k-steps (64 elements) in the last, possibly partial, stage
   const int ksteps_total = (p.K + 63) / 64;
 
@@ -123,8 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_b = p.transposed ? policy_evict_last() : policy_evict_first();
       uint32_t stage = 0, phase = 0, issued = 0, issued_par = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
+      WorkIter wi(p, blockIdx.x, gridDim.x);
+      Seg w;
+      while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x201u, abort_flag)) { ok = false; break; }
           // scale atoms of this stage that exist (a partial last stage has fewer)
@@ -157,8 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t sf_base = tmem_base + 2 * BN;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
+      WorkIter wi(p, blockIdx.x, gridDim.x);
+      Seg w;
+      while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
         if (!mbar_wait(tempty(acc), acc_phase ^ 1u, p.err, 0x202u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -206,15 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int quarter = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+    WorkIter wi(p, blockIdx.x, gridDim.x);
+    Seg w;
+    while (wi.next(p, blockIdx.x, gridDim.x, w)) {
       if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
       tc_fence_after();
       epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (p.splits > 1) splitk_finish<BN>(p, w, quarter, lane);
+      if (!w.full) streamk_finish<BN>(p, w, quarter, lane);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -238,40 +240,17 @@ lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const ui
 
 }  // namespace
 
-// FP4 plan: always 128 x 128 tiles on the natural operands (no swap; the
-// scale layouts of A and B are the same 128-row tiles).  Split-K when the
-// tiles leave SMs idle and a workspace is given.
+// FP4 plan: 128 x 128 tiles on the natural operands (no swap; the scale
+// layouts of A and B are the same 128-row tiles); stream-K when a workspace is
+// given and the tiles do not divide evenly over the SMs.
 Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes) {
   Fp8Plan pl{};
   pl.transposed = 0;
   pl.bn = 128;
   pl.I = M;
   pl.J = N;
-  pl.i_tiles = static_cast<int>((M + kBM - 1) / kBM);
-  pl.j_tiles = static_cast<int>((N + pl.bn - 1) / pl.bn);
   pl.kblocks = static_cast<int>((K + kKPerStage - 1) / kKPerStage);
-  const int tiles = pl.i_tiles * pl.j_tiles;
-  const int sms = sm_count();
-  pl.splits = 1;
-  if (have_ws && tiles < sms * 4) {
-    double best = static_cast<double>(tiles) / (((tiles + sms - 1) / sms) * static_cast<double>(sms));
-    for (int s = 2; s <= 32; ++s) {
-      const int per = (pl.kblocks + s - 1) / s;
-      if (per < 4) break;
-      const int real = (pl.kblocks + per - 1) / per;
-      const int units = tiles * real;
-      const double eff = static_cast<double>(units) / (((units + sms - 1) / sms) * static_cast<double>(sms));
-      if (fp8_ws_bytes(tiles, real, pl.bn) > ws_bytes) continue;
-      if (eff > best + 0.02) {
-        best = eff;
-        pl.splits = real;
-      }
-    }
-  }
-  pl.kb_per_split = (pl.kblocks + pl.splits - 1) / pl.splits;
-  pl.splits = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
-  pl.units = tiles * pl.splits;
-  pl.grid = std::min(pl.units, sms);
+  finish_plan(pl, have_ws, ws_bytes);
   return pl;
 }
 
@@ -282,10 +261,9 @@ lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const 
   p.i_tiles = pl.i_tiles;
   p.j_tiles = pl.j_tiles;
   p.kblocks = pl.kblocks;
-  p.splits = pl.splits;
-  p.kb_per_split = pl.kb_per_split;
+  p.streamk = pl.streamk;
   p.transposed = 0;
-  if (pl.splits > 1) {
+  if (pl.streamk) {
     const int tiles = pl.i_tiles * pl.j_tiles;
     const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
     p.counters = static_cast<int*>(ws);

@@ -11,8 +11,9 @@
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one thread),
 //               accumulating a 128 x BN fp32 tile into one of two TMEM
 //               buffers, so the epilogue of tile t overlaps the K loop of t+1;
-//   warps 2-5   epilogue: tcgen05.ld -> scales -> bf16 -> global (or split-K
-//               partials + an in-order reduction by the last split).
+//   warps 2-5   epilogue: tcgen05.ld -> scales -> bf16 -> global (or, for a
+//               stream-K piece, partial sums + an in-order combination by the
+//               last contributor of the tile).
 // Every barrier wait is bounded (a timeout sets the device error word and the
 // kernel winds down); no trap, no unbounded spin.
 #include <cuda_runtime.h>
@@ -92,8 +93,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int units = p.i_tiles * p.j_tiles * p.splits;
-
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
@@ -102,8 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_par = 0;   // per-stage: issued at least once / parity of last issue
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
+      WorkIter wi(p, blockIdx.x, gridDim.x);
+      Seg w;
+      while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x101u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(full(stage), C::kStageBytes);
@@ -126,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // --------------------------------------------------------------- MMA
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
+      WorkIter wi(p, blockIdx.x, gridDim.x);
+      Seg w;
+      while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
         if (!mbar_wait(tempty(acc), acc_phase ^ 1u, p.err, 0x102u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -158,15 +159,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+    WorkIter wi(p, blockIdx.x, gridDim.x);
+    Seg w;
+    while (wi.next(p, blockIdx.x, gridDim.x, w)) {
       if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x104u, abort_flag)) break;
       tc_fence_after();
       epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (p.splits > 1) splitk_finish<BN>(p, w, quarter, lane);
+      if (!w.full) streamk_finish<BN>(p, w, quarter, lane);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -190,56 +192,46 @@ lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmP
 
 }  // namespace
 
-// Tile/split choice: swap-AB (weights on the tensor core's M side) when the
-// token count fits one N tile (<= 256), otherwise 128 x 256 tiles.  Split-K
-// is used when the tiles alone leave SMs idle and a workspace is available.
+// Tile choice: swap-AB (weights on the tensor core's M side) when the token
+// count fits one N tile (<= 256), otherwise 128 x 256 tiles.  Stream-K (equal
+// K-iteration ranges per CTA, partial tiles combined in a fixed order) when a
+// workspace is given and whole tiles would not divide evenly over the SMs.
 Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes) {
   Fp8Plan pl{};
   pl.transposed = (M <= 256);
-  const int64_t I = pl.transposed ? N : M;
-  const int64_t J = pl.transposed ? M : N;
+  pl.I = pl.transposed ? N : M;
+  pl.J = pl.transposed ? M : N;
   int bn = 256;
   if (pl.transposed) {
     bn = 16;
-    while (bn < J) bn *= 2;
+    while (bn < pl.J) bn *= 2;
   }
   pl.bn = bn;
-  pl.I = I;
-  pl.J = J;
-  pl.i_tiles = static_cast<int>((I + kBM - 1) / kBM);
-  pl.j_tiles = static_cast<int>((J + bn - 1) / bn);
   pl.kblocks = static_cast<int>((K + kBKBytes - 1) / kBKBytes);
-  const int tiles = pl.i_tiles * pl.j_tiles;
-  const int sms = sm_count();
-  pl.splits = 1;
-  if (have_ws_budget && tiles < sms * 4) {
-    // pick the split count (>= 4 K blocks each) with the best wave efficiency
-    double best = static_cast<double>(tiles) / (((tiles + sms - 1) / sms) * static_cast<double>(sms));
-    for (int s = 2; s <= 32; ++s) {
-      const int per = (pl.kblocks + s - 1) / s;
-      if (per < 4) break;
-      const int real = (pl.kblocks + per - 1) / per;
-      const int units = tiles * real;
-      const double eff = static_cast<double>(units) / (((units + sms - 1) / sms) * static_cast<double>(sms));
-      const size_t need = fp8_ws_bytes(tiles, real, bn);
-      if (need > ws_bytes) continue;
-      if (eff > best + 0.02) {
-        best = eff;
-        pl.splits = real;
-      }
-    }
-  }
-  pl.kb_per_split = (pl.kblocks + pl.splits - 1) / pl.splits;
-  pl.splits = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
-  pl.units = tiles * pl.splits;
-  pl.grid = std::min(pl.units, sms);
+  finish_plan(pl, have_ws_budget, ws_bytes);
   return pl;
 }
 
-size_t fp8_ws_bytes(int tiles, int splits, int bn) {
-  if (splits <= 1) return 0;
-  const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
-  return counters + static_cast<size_t>(tiles) * splits * 128 * bn * sizeof(float);
+void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
+  pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
+  pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
+  const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
+  const int sms = sm_count();
+  pl.streamk = 0;
+  pl.grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+  if (have_ws && tiles % sms != 0) {
+    Fp8Plan sk = pl;
+    sk.streamk = 1;
+    sk.grid = static_cast<int>(std::min<int64_t>(tiles * pl.kblocks, sms));
+    if (plan_ws_bytes(sk) <= ws_bytes) pl = sk;
+  }
+}
+
+size_t plan_ws_bytes(const Fp8Plan& pl) {
+  if (!pl.streamk) return 0;
+  const size_t tiles = static_cast<size_t>(pl.i_tiles) * pl.j_tiles;
+  const size_t counters = (tiles * 4 * sizeof(int) + 255) / 256 * 256;
+  return counters + static_cast<size_t>(pl.grid) * 2 * 128 * pl.bn * sizeof(float);
 }
 
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
@@ -249,10 +241,9 @@ lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const 
   p.i_tiles = pl.i_tiles;
   p.j_tiles = pl.j_tiles;
   p.kblocks = pl.kblocks;
-  p.splits = pl.splits;
-  p.kb_per_split = pl.kb_per_split;
+  p.streamk = pl.streamk;
   p.transposed = pl.transposed;
-  if (pl.splits > 1) {
+  if (pl.streamk) {
     const int tiles = pl.i_tiles * pl.j_tiles;
     const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
     p.counters = static_cast<int*>(ws);

@@ -17,16 +17,25 @@ struct Fp8Plan {
   int transposed;     // swap-AB: weights on the tensor core's M side
   int bn;             // N tile of the tensor core
   int64_t I, J;       // rows of the A / B operands
-  int i_tiles, j_tiles, kblocks, splits, kb_per_split, units, grid;
+  int i_tiles, j_tiles, kblocks;
+  int streamk;        // 1: equal K-iteration ranges per CTA (needs a workspace)
+  int grid;
 };
 
 Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes);
-size_t fp8_ws_bytes(int tiles, int splits, int bn);
+// workspace a plan needs (0 for data-parallel plans): tile counters + two
+// partial-sum slots per CTA
+size_t plan_ws_bytes(const Fp8Plan& pl);
+// fill in tile counts / stream-K choice / grid for the given tiling
+void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st);
 
 lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
                             const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
+
+lpq_status launch_int8(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
+                       const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
 
 Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes);
 lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa,

@@ -1,5 +1,5 @@
 // gemm_noalloc.cu - lpq_gemm_scaled_noalloc: the FP8 row-scaled GEMM with
-// its split-K scratch taken from a fixed array inside the library instead of
+// its stream-K scratch taken from a fixed array inside the library instead of
 // a caller-provided workspace.
 //
 // Who needs this: a caller that cannot allocate device memory for a
@@ -8,7 +8,7 @@
 // the tensors of the operation, or a latency-critical path where cudaMalloc's
 // implicit device-wide synchronisation is not acceptable and no workspace was
 // reserved ahead of time.  Such a caller still passes its inputs and outputs;
-// only the split-K partial sums and tile counters live here.
+// only the stream-K partial sums and tile counters live here.
 //
 // The scratch is a file-scope __device__ array of LPQ_NOALLOC_SCRATCH_BYTES
 // (16 MiB).  Every GPU that loads the library holds it until the process
@@ -85,14 +85,14 @@ lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream) {
 
   // the tiling lpq_gemm_scaled would use with a large enough workspace
   const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX);
-  const size_t need = fp8_ws_bytes(pl.i_tiles * pl.j_tiles, pl.splits, pl.bn);
+  const size_t need = plan_ws_bytes(pl);
   if (need > kNoallocScratchBytes) return LPQ_ERR_WORKSPACE;   // problem needs more than the built-in scratch
 
   void* scratch = nullptr;
   lpq_status s = scratch_ptr(&scratch);
   if (s != LPQ_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (pl.splits > 1) {
+  if (pl.streamk) {
     // tile counters must start at zero; a wound-down earlier call may have left them set
     const size_t counters = (static_cast<size_t>(pl.i_tiles) * pl.j_tiles * 4 * sizeof(int) + 255) / 256 * 256;
     cudaError_t e = cudaMemsetAsync(scratch, 0, counters, st);
@@ -115,7 +115,7 @@ lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream) {
   p.Y = d->Y;
   p.ldy = d->ldy;
   p.err = error_word_ptr();
-  return launch_fp8_rowscale(pl, tmA, tmB, p, pl.splits > 1 ? scratch : nullptr, st);
+  return launch_fp8_rowscale(pl, tmA, tmB, p, pl.streamk ? scratch : nullptr, st);
 }
 
 }  // extern "C"
