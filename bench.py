@@ -70,8 +70,9 @@ class GraphEvents:
         self.events.append(e)
         return e
 
-    def record(self, ev, stream):
-        r = self.rt.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), 1)
+    def record(self, ev, stream, external=True):
+        # cudaEventRecordExternal (1) only inside a capture; a plain record otherwise
+        r = self.rt.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), 1 if external else 0)
         if r != 0:
             raise RuntimeError(f"cudaEventRecordWithFlags failed ({r})")
 
@@ -99,7 +100,7 @@ def load_peaks():
 
 
 # nominal dense ratios to bf16 (2.25 PF): FP8 4.5 -> 2x, FP4 13.5 -> 6x
-NOMINAL_RATIO = {"fp8": 2.0, "fp4": 6.0, "bf16": 1.0}
+NOMINAL_RATIO = {"fp8": 2.0, "fp4": 6.0, "bf16": 1.0, "int8": 2.0}
 
 
 # ----------------------------------------------------------------- clocks --
@@ -191,7 +192,8 @@ def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
             sx = torch.empty((M,), dtype=torch.float32, device="cuda")
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
-            desc = L.make_desc(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws)
+            desc = L.make_desc(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws,
+                               flags=L.GEMM_B_STATIC)   # weights quantized at load time
             W.keep = getattr(W, "keep", []) + [Wq, sw, ws]
             W.calls.append(dict(kind="quant_fp8_row", M=M, K=K, N=N,
                                 fn=(lambda Xd=Xd, Xq=Xq, sx=sx: L.lpq_quantize_act_fp8(Xd, L.GRAN_ROW, Xq, sx)),
@@ -249,8 +251,91 @@ def build_fp4(L, torch, wl):
     return W
 
 
+def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
+    """FP8 prefill with 1x128 activation / 128x128 weight block scales."""
+    W = Workload(wl.name, L, torch)
+    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "act": "fp8 e4m3 per 1x128 group, dynamic", "weight": "fp8 e4m3 per 128x128 block",
+                "l2": "inputs larger than L2 (M=8192 activations 64-235 MB bf16; weights 17-117 MB fp8)"}
+    W.dominant = "gemm_fp8_block"
+    W.dominant_bound = "tensor"
+    W.dominant_dtype = "fp8"
+    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    wq = {}
+    for si, (K, N) in enumerate(wl.KNs):
+        Wd = W.dev_bf16(CFG.make_w(wl, N, K, salt=si))
+        wq[si] = L.quantize_weight_fp8(Wd, L.GRAN_BLOCK_128x128)
+        del Wd
+    for mi, M in enumerate(wl.Ms):
+        for si, (K, N) in enumerate(wl.KNs):
+            Wq, sw = wq[si]
+            xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
+            Xd = W.dev_bf16(xb)
+            Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            sx = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            desc = L.make_desc(L.FMT_FP8, L.GRAN_BLOCK_1x128, L.GRAN_BLOCK_128x128, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
+            W.keep = getattr(W, "keep", []) + [desc]
+            W.calls.append(dict(kind="quant_fp8_1x128", M=M, K=K, N=N,
+                                fn=(lambda Xd=Xd, Xq=Xq, sx=sx: L.lpq_quantize_act_fp8(Xd, L.GRAN_BLOCK_1x128, Xq, sx)),
+                                bytes=M * K * 3 + 4 * M * K // 128, flops=0))
+            W.calls.append(dict(kind="gemm_fp8_block", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
+                                bytes=(M + N) * K + 2 * M * N, flops=2 * M * N * K))
+            W.dev_in.append(Xd)
+            W.dev_out.append(Y)
+            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
+            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+    return W
+
+
+def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
+    """INT8 W8A8 with SmoothQuant: calibration and smoothed weight
+    quantization at load; per step the smoothed per-token quantizer and the
+    INT8 GEMM."""
+    W = Workload(wl.name, L, torch)
+    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "alpha": CFG.SMOOTH_ALPHA, "calibration_tokens": CFG.INT8_CALIB_TOKENS,
+                "l2": "inputs larger than L2 for M=4096 (W 16-117 MB int8, X 32 MB bf16)"}
+    W.dominant = "gemm_int8"
+    W.dominant_bound = "tensor"
+    W.dominant_dtype = "int8"
+    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    K = wl.KNs[0][0]
+    amax = torch.zeros(K, dtype=torch.float32, device="cuda")
+    L.lpq_act_absmax_update(W.dev_bf16(CFG.make_calib(wl, K)), amax)
+    wq = {}
+    for si, (K, N) in enumerate(wl.KNs):
+        Wd = W.dev_bf16(CFG.make_w(wl, N, K, salt=si))
+        sm = L.smooth_calibrate(amax, Wd, CFG.SMOOTH_ALPHA)
+        Wq, sw = L.quantize_weight_int8(Wd, sm)
+        wq[si] = (Wq, sw, sm)
+        del Wd
+    for mi, M in enumerate(wl.Ms):
+        for si, (K, N) in enumerate(wl.KNs):
+            Wq, sw, sm = wq[si]
+            xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
+            Xd = W.dev_bf16(xb)
+            Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+            sx = torch.empty((M,), dtype=torch.float32, device="cuda")
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            desc = L.make_desc(L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
+            W.keep = getattr(W, "keep", []) + [desc]
+            W.calls.append(dict(kind="quant_int8_smooth", M=M, K=K, N=N,
+                                fn=(lambda Xd=Xd, Xq=Xq, sx=sx, sm=sm: L.lpq_quantize_act_int8(Xd, sm, Xq, sx)),
+                                bytes=M * K * 3 + 4 * M, flops=0))
+            W.calls.append(dict(kind="gemm_int8", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
+                                bytes=(M + N) * K + 4 * (M + N) + 2 * M * N, flops=2 * M * N * K))
+            W.dev_in.append(Xd)
+            W.dev_out.append(Y)
+            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
+            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+    return W
+
+
 BUILDERS = {
     "decode_fp8": lambda L, t: build_decode_fp8(L, t),
+    "prefill_fp8_block": lambda L, t: build_prefill_block(L, t),
+    "int8_smoothquant": lambda L, t: build_int8(L, t),
     "nvfp4": lambda L, t: build_fp4(L, t, CFG.NVFP4_W4A4),
     "mxfp4": lambda L, t: build_fp4(L, t, CFG.MXFP4_W4A4),
 }
@@ -264,9 +349,10 @@ def oracle_sample(workload: str, budget_s: float = 15.0):
     threads)."""
     from oracle import quant as Q
     from oracle import gemm as G
-    wl = {"decode_fp8": CFG.DECODE_FP8, "nvfp4": CFG.NVFP4_W4A4, "mxfp4": CFG.MXFP4_W4A4}[workload]
+    wl = {"decode_fp8": CFG.DECODE_FP8, "nvfp4": CFG.NVFP4_W4A4, "mxfp4": CFG.MXFP4_W4A4,
+          "prefill_fp8_block": CFG.PREFILL_FP8_BLOCK, "int8_smoothquant": CFG.INT8_SMOOTHQUANT}[workload]
     n_rows = 64
-    Ms = [m for m in wl.Ms if m <= 512] or [wl.Ms[0]]
+    Ms = [m for m in wl.Ms if m <= 512] or [min(wl.Ms)]
     flops, t_total, done = 0, 0.0, 0
     for mi, M in enumerate(Ms):
         for si, (K, N) in enumerate(wl.KNs):
@@ -274,7 +360,20 @@ def oracle_sample(workload: str, budget_s: float = 15.0):
             wb = CFG.make_w(wl, n_rows, K, salt=si)
             x = synth.f32_from_bf16_bits(xb)
             w = synth.f32_from_bf16_bits(wb)
-            if wl.fmt == "fp8":
+            if wl.fmt == "fp8_block":
+                qw, sw = Q.fp8_per_block_128x128_ragged(w)      # load time, untimed
+                t0 = time.perf_counter()
+                qx, sx = Q.fp8_per_group_1x128(x)
+                from oracle import codecs as Cd
+                xh = (Cd.e4m3fn_decode(qx).reshape(M, K // 128, 128) * sx[..., None]).reshape(M, K)
+                wh = (Cd.e4m3fn_decode(qw).reshape(n_rows, K // 128, 128) * sw[0][None, :, None]).reshape(n_rows, K)
+                G.matmul_ref(xh, wh)
+            elif wl.fmt == "int8":
+                qw, sw = Q.int8_per_row(w, None, weight=True)
+                t0 = time.perf_counter()
+                qx, sx = Q.int8_per_row(x)
+                G.int8_epilogue_fp32(G.int8_exact(qx, qw), sx, sw)
+            elif wl.fmt == "fp8":
                 qw, sw = Q.fp8_per_row(w)                       # load time, untimed
                 t0 = time.perf_counter()
                 qx, sx = Q.fp8_per_row(x)
@@ -381,60 +480,86 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # ---- the K timed steps, captured once into a CUDA graph (the library's
-    # calls are plain stream work, so capture records them as kernel nodes);
-    # per-launch timing events are event-record nodes inside the graph
+    # ---- CUDA graphs (the library's calls are plain stream work, so stream
+    # capture records them as kernel nodes; consecutive kernels overlap their
+    # launch through programmatic dependent launch):
+    #   g_run  the K steps exactly as timed (no extra nodes),
+    #   g_dom  the K steps' launches of the dominant kernel only (its average
+    #          launch duration for the roofline),
+    #   g_ins  the K steps with a timing-event node around every launch (the
+    #          per-kernel table; the events themselves serialise the kernels).
     GE = GraphEvents()
     evs = [[(GE.new(), GE.new()) for _ in W.calls] for _ in range(args.steps)]
     cap = torch.cuda.Stream()
 
-    def timed_steps(on):
+    def run_steps():
+        for _ in range(args.steps):
+            step()
+
+    def dom_steps():
+        for _ in range(args.steps):
+            for c in W.calls:
+                if c["kind"] == W.dominant:
+                    c["fn"]()
+
+    def ins_steps(on, external=True):
         for s_ in range(args.steps):
             for i, c in enumerate(W.calls):
-                GE.record(evs[s_][i][0], on)
+                GE.record(evs[s_][i][0], on, external)
                 c["fn"]()
-                GE.record(evs[s_][i][1], on)
+                GE.record(evs[s_][i][1], on, external)
 
-    graph = None
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+        stream.wait_stream(cap)
+        g.replay()                      # one untimed replay of each graph
+        torch.cuda.synchronize()
+        return g
+
+    g_run = g_dom = g_ins = None
     if not args.eager:
         try:
-            cap.wait_stream(stream)
-            graph = torch.cuda.CUDAGraph()
             L.lpq_reset_launch_count()
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(graph, stream=cap):
-                    timed_steps(cap)
-            stream.wait_stream(cap)
-            launches = L.lpq_launch_count()   # library kernels in the graph = launches in the timed region
-            graph.replay()                    # one untimed replay of the graph itself
-            torch.cuda.synchronize()
+            g_run = capture(run_steps)
+            launches = L.lpq_launch_count()   # library kernels in the timed graph
+            g_dom = capture(dom_steps)
+            g_ins = capture(lambda: ins_steps(cap))
         except Exception as e:  # capture unavailable: time the same calls eagerly
             print(f"bench: graph capture failed ({e}); timing eagerly", file=sys.stderr)
-            graph = None
+            g_run = g_dom = g_ins = None
             torch.cuda.synchronize()
+
+    def timed(fn_graph, fn_eager):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if fn_graph is not None:
+            fn_graph.replay()
+        else:
+            fn_eager()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if graph is None:
+    if g_run is None:
         L.lpq_reset_launch_count()
-    t_start.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        timed_steps(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if graph is None:
+    ms_total = timed(g_run, run_steps)           # <- the timed region: K steps
+    if g_run is None:
         launches = L.lpq_launch_count()
     if dist:
         dist.barrier()
+    ms_dom = timed(g_dom, dom_steps)
+    timed(g_ins, lambda: ins_steps(stream, external=False))
     clocks = clk.stop()
-    ms_total = t_start.elapsed_time(t_end)
     if dist:
         tt = torch.tensor([ms_total], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -444,7 +569,7 @@ def main():
     flops_step = sum(c["flops"] for c in W.calls)
     value = flops_step * world / (ms_step * 1e-3) / 1e12
 
-    # per-kernel statistics from the in-region events
+    # per-kernel statistics from the instrumented replay
     kinds = {}
     for s in range(args.steps):
         for i, c in enumerate(W.calls):
@@ -463,7 +588,8 @@ def main():
                       "GB/s": k["bytes"] / (k["launch_ms"] * 1e-3) / 1e9,
                       "TFLOP/s": k["flops"] / (k["launch_ms"] * 1e-3) / 1e12 if k["flops"] else 0.0,
                       "share": k["launch_ms"] / sum(v["launch_ms"] for n, v in kinds.items() if "[" not in n)}
-    dom = kinds[W.dominant]
+    dom = dict(kinds[W.dominant])
+    dom["launch_ms"] = ms_dom          # all dominant launches of K steps, back to back, no inner events
     if W.dominant_bound == "hbm":
         achieved = dom["bytes"] / (dom["launch_ms"] * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
@@ -475,7 +601,10 @@ def main():
                 "frac": achieved / peak,
                 "peak_src": f"{peaks['src']} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops x nominal ratio'})",
                 "traffic": None,
-                "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"]}
+                "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"],
+                "algorithmic_flops_per_launch": dom["flops"] / dom["launches"],
+                "avg_launch_us": 1000 * ms_dom / dom["launches"],
+                "timing": "CUDA events around a graph replay of the K steps' launches of this kernel only"}
 
     # ---- end to end through the C ABI with host buffers (pinned): every step
     # copies its activations in and its Y out; the calls are captured in a
@@ -492,18 +621,10 @@ def main():
             for h, d in zip(W.host_out, W.dev_out):
                 h.copy_(d, non_blocking=True)
 
-    g2 = None
-    if graph is not None:
-        g2 = torch.cuda.CUDAGraph()
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g2, stream=cap):
-                e2e_steps()
-        stream.wait_stream(cap)
-        g2.replay()
-    else:
+    g2 = capture(e2e_steps) if g_run is not None else None
+    if g2 is None:
         e2e_steps()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_s.record(stream)
     if g2 is not None:
@@ -525,6 +646,8 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": {"decode_fp8": "fp8-e4m3 (fp32 accum)",
+                                               "prefill_fp8_block": "fp8-e4m3 block-scaled (fp32 accum)",
+                                               "int8_smoothquant": "int8 (int32 accum)",
                                                "nvfp4": "nvfp4-e2m1 (fp32 accum)",
                                                "mxfp4": "mxfp4-e2m1 (fp32 accum)"}[args.workload],
                 "data": "synthetic (seeded, pages' shapes and outlier mix)",
@@ -533,7 +656,8 @@ def main():
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "clocks": clocks,
-                "launch_mode": "cuda-graph replay" if graph is not None else "eager"}
+                "launch_mode": "cuda-graph replay" if g_run is not None else "eager",
+                "kernel_table_timing": "per-launch event nodes in a replay after the timed region (adds a few us per launch)"}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -189,7 +189,14 @@ typedef struct {
   const float* gb;             /* NVFP4 tensor scale of B (device, [1])       */
   uint16_t* Y; int64_t ldy;    /* bf16 output                                 */
   void* workspace; size_t workspace_bytes;
+  uint32_t flags;              /* LPQ_GEMM_* bits below; 0 = none          */
 } lpq_gemm_desc;
+
+/* flags: the weights B are not written by the kernel that immediately
+ * precedes this call on the stream (true for weights quantized at load time).
+ * The GEMM may then start streaming B before that kernel has finished; its
+ * activations, scales and output still wait for it.  FP8 row-scaled GEMMs. */
+#define LPQ_GEMM_B_STATIC 1u
 
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d);
 lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream);

@@ -134,3 +134,28 @@ def test_fp8_end_to_end_quantize_then_gemm():
     yr, b = _ref(qxo, sxo, qwo, swo)
     ok, worst = G.check(bf16_to_f64(host(Y)), yr, b)
     assert ok.all(), worst
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (16, 4096, 14336), (256, 6144, 4096)])
+def test_fp8_static_weights_flag(M, N, K):
+    """LPQ_GEMM_B_STATIC lets the GEMM stream its weights while the activation
+    quantizer launched just before it is still running; results must be
+    identical to the unflagged call and within tolerance of the oracle."""
+    L = lpq()
+    xb = synth.activations(M, K, 900 + M, n_outlier=max(1, K // 1000), lo=50, hi=500)
+    wb = synth.weights(N, K, 901)
+    Wq, sw = L.quantize_weight_fp8(dev_bf16(wb), L.GRAN_ROW)
+    X = dev_bf16(xb)
+    ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
+    outs = []
+    for flags in (0, L.GEMM_B_STATIC, L.GEMM_B_STATIC):
+        qx, sx = L.quantize_act_fp8(X, L.GRAN_ROW)
+        outs.append(L.gemm_scaled(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, qx, Wq, sx, sw, M=M, N=N, K=K,
+                                  workspace=ws, flags=flags))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    qxo, sxo = Q.fp8_per_row(synth.f32_from_bf16_bits(xb))
+    qwo, swo = Q.fp8_per_row(synth.f32_from_bf16_bits(wb))
+    yr, b = _ref(qxo, sxo, qwo, swo)
+    ok, worst = G.check(bf16_to_f64(host(outs[1])), yr, b)
+    assert ok.all(), worst

@@ -20,13 +20,15 @@ struct GemmParams {
   int i_tiles, j_tiles;        // tiles of 128 rows of A, BN rows of B
   int kblocks;                 // K blocks (one pipeline stage each)
   int streamk;                 // 0: whole tiles round-robin; 1: equal K-iteration ranges per CTA
+  int b_static;                // weights not written by the previous kernel: may be read before its end
+  int j_fast;                  // tile order: 1 = consecutive tiles share the A rows (i), 0 = share B rows (j)
   int transposed;              // 0: Y[i][j], 1: Y[j][i]
   // epilogue scales: y = (acc * s_x) * s_w, s_x / s_w read from the i or j side
   const float* sx; int sx_stride;                // sx_stride 0: one scale for all
   const float* sw; int sw_stride;
   const float* gx; const float* gw;              // optional extra factors (NVFP4 g)
   uint16_t* Y; int64_t ldy;
-  float* ws;                   // stream-K partials [grid][2][128][BN]
+  float* ws;                   // stream-K partials [grid][2][BN/4][128][4]
   int* counters;               // [tiles * 4], zero on entry, zero on exit
   uint32_t* err;
 };
@@ -72,8 +74,13 @@ struct WorkIter {
       s.kb1 = static_cast<int>(s.kb0 + left < p.kblocks ? s.kb0 + left : p.kblocks);
       it += s.kb1 - s.kb0;
     }
-    s.i_tile = s.tile % p.i_tiles;
-    s.j_tile = s.tile / p.i_tiles;
+    if (p.j_fast) {
+      s.j_tile = s.tile % p.j_tiles;
+      s.i_tile = s.tile / p.j_tiles;
+    } else {
+      s.i_tile = s.tile % p.i_tiles;
+      s.j_tile = s.tile / p.i_tiles;
+    }
     s.full = (s.kb0 == 0 && s.kb1 == p.kblocks);
     s.g_first = g;
     s.n_contrib = 1;
@@ -160,8 +167,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
   const int row_in_tile = quarter * 32 + lane;
   const int i = w.i_tile * 128 + row_in_tile;
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
+  // partial slot layout [BN/4][128][4]: for one group of 4 columns the 32
+  // lanes of a warp touch 512 contiguous bytes
   float* part = w.full ? nullptr
-                       : p.ws + ((static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 + row_in_tile) * BN;
+                       : p.ws + (static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 * BN + row_in_tile * 4;
 #pragma unroll 1
   for (int c = 0; c < BN; c += CW) {
     float v[CW];
@@ -183,7 +192,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
     } else {
 #pragma unroll
       for (int t = 0; t < CW; t += 4)
-        __stcg(reinterpret_cast<float4*>(part + c + t), make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
+        __stcg(reinterpret_cast<float4*>(part + static_cast<int64_t>((c + t) / 4) * 512),
+               make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]));
     }
   }
 }
@@ -209,7 +219,7 @@ __device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w
   __threadfence();
   const int row_in_tile = quarter * 32 + lane;
   const int i = w.i_tile * 128 + row_in_tile;
-  const int64_t row_off = static_cast<int64_t>(row_in_tile) * BN;
+  const int64_t row_off = static_cast<int64_t>(row_in_tile) * 4;
 #pragma unroll 2
   for (int c = 0; c < BN; c += kSub) {
     float v[kSub];
@@ -222,10 +232,10 @@ __device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w
         if (s0 + b < w.n_contrib) {
           const int g = w.g_first + s0 + b;
           const int slot = (s0 + b == 0) ? 1 : 0;
-          const float4* part = reinterpret_cast<const float4*>(
-              p.ws + (static_cast<int64_t>(g) * 2 + slot) * 128 * BN + row_off + c);
-          f[b][0] = __ldcg(part);
-          f[b][1] = __ldcg(part + 1);
+          const float* part = p.ws + (static_cast<int64_t>(g) * 2 + slot) * 128 * BN + row_off +
+                              static_cast<int64_t>(c / 4) * 512;
+          f[b][0] = __ldcg(reinterpret_cast<const float4*>(part));
+          f[b][1] = __ldcg(reinterpret_cast<const float4*>(part + 512));
         }
       }
 #pragma unroll

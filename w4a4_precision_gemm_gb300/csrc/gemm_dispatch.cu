@@ -56,7 +56,7 @@ lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st) {
   p.Y = d->Y;
   p.ldy = d->ldy;
   p.err = error_word_ptr();
-  return launch_fp8_rowscale(pl, tmA, tmB, p, d->workspace, st);
+  return launch_fp8_rowscale(pl, tmA, tmB, p, d->workspace, st, (d->flags & LPQ_GEMM_B_STATIC) != 0);
 }
 
 bool is_fp8_block(const lpq_gemm_desc* d) {

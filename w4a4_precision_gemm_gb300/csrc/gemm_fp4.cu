@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();      // inputs of this call may come from the previous kernel
+  pdl_launch();
   // MMA k-steps (64 elements) in the last, possibly partial, stage
   const int ksteps_total = (p.K + 63) / 64;
 
@@ -234,8 +236,8 @@ lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const ui
   static uint64_t done_mask = 0;
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp4_kernel<BN, NV>), C::kSmemBytes, &done_mask);
   if (s != LPQ_OK) return s;
-  gemm_fp4_kernel<BN, NV><<<grid, kThreads, C::kSmemBytes, st>>>(tmA, tmB, sfa, sfb, kb4, p);
-  return after_launch();
+  return launch_pdl(gemm_fp4_kernel<BN, NV>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, tmA, tmB, sfa, sfb, kb4,
+                    p);
 }
 
 }  // namespace

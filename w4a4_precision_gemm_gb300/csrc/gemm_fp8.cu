@@ -34,8 +34,11 @@ constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
 
 template <int BN>
 struct Fp8Cfg {
+  // small token tiles (decode): two CTAs share an SM (two independent TMA
+  // streams per SM, and one CTA's epilogue overlaps the other's loads)
+  static constexpr int kCtasPerSm = (BN <= 64) ? 2 : 1;
   static constexpr int kStageBytes = (kBM + BN) * kBKBytes;
-  static constexpr int kStages = cmin(12, (200 * 1024) / kStageBytes);
+  static constexpr int kStages = cmin(12, (kCtasPerSm == 2 ? 108 * 1024 : 200 * 1024) / kStageBytes);
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
   // instruction descriptor: D fp32, A/B E4M3, K-major both, N = BN, M = 128
@@ -43,8 +46,12 @@ struct Fp8Cfg {
       (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 };
 
+static_assert(Fp8Cfg<64>::kCtasPerSm == 2 && Fp8Cfg<128>::kCtasPerSm == 1, "planner assumes 2 CTAs/SM for BN <= 64");
+static_assert(2 * Fp8Cfg<64>::kSmemBytes <= 227 * 1024, "two CTAs must fit one SM's shared memory");
+static_assert(2 * Fp8Cfg<16>::kSmemBytes <= 227 * 1024, "two CTAs must fit one SM's shared memory");
+
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
     gemm_fp8_rowscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const GemmParams p) {
   using C = Fp8Cfg<BN>;
@@ -92,6 +99,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Inputs of this call may come from the previous kernel on the stream:
+  // every thread waits for it before touching global memory, except the TMA
+  // thread when the weights are declared static, which first starts the
+  // weight stream of its opening stages (see the producer below).
+  const bool early_w = p.b_static && warp == 0 && lane == 0;
+  if (!early_w) {
+    pdl_wait();
+    pdl_launch();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -103,12 +119,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       WorkIter wi(p, blockIdx.x, gridDim.x);
       Seg w;
+      // static weights: claim the first (still free) stages and start their
+      // weight tiles before waiting for the previous kernel; the token tiles of
+      // those stages follow after the wait
+      int pre = 0;
+      if (early_w) {
+        WorkIter wi2 = wi;
+        Seg w2;
+        bool h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
+        int kb2 = h2 ? w2.kb0 : 0;
+        while (h2 && pre < S) {
+          mbar_arrive_expect_tx(full(pre), C::kStageBytes);
+          if (p.transposed)
+            tma_load_2d(smem_u32(sA + pre * kBM * kBKBytes), &tmA, full(pre), kb2 * kBKBytes, w2.i_tile * kBM, pol_a);
+          else
+            tma_load_2d(smem_u32(sB + pre * BN * kBKBytes), &tmB, full(pre), kb2 * kBKBytes, w2.j_tile * BN, pol_b);
+          ++pre;
+          if (++kb2 == w2.kb1) {
+            h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
+            if (h2) kb2 = w2.kb0;
+          }
+        }
+        pdl_wait();
+        pdl_launch();
+      }
+      int n = 0;                              // stages handled so far
       while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x101u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(full(stage), C::kStageBytes);
-          tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
-          tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++n) {
+          if (n < pre) {
+            // weight tile already on its way; add the token tile
+            if (p.transposed)
+              tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+            else
+              tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+          } else {
+            if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x101u, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(full(stage), C::kStageBytes);
+            tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+            tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+          }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -186,16 +235,17 @@ lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmP
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes,
                                   &done_mask);
   if (s != LPQ_OK) return s;
-  gemm_fp8_rowscale_kernel<BN><<<grid, kThreads, C::kSmemBytes, st>>>(tmA, tmB, p);
-  return after_launch();
+  return launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, tmA, tmB, p);
 }
 
 }  // namespace
 
-// Tile choice: swap-AB (weights on the tensor core's M side) when the token
-// count fits one N tile (<= 256), otherwise 128 x 256 tiles.  Stream-K (equal
-// K-iteration ranges per CTA, partial tiles combined in a fixed order) when a
-// workspace is given and whole tiles would not divide evenly over the SMs.
+// Tile choice: swap-AB (weights on the tensor core's M side) for <= 256
+// tokens: N tile = the token count rounded up to 16 up to 64 tokens, 64 above
+// (several token tiles share each weight tile, visited back to back so the
+// weight rows are re-read from L2).  More tokens: 128 x 256 tiles.  Stream-K
+// (equal K-iteration ranges per CTA, partial tiles combined in a fixed order)
+// when a workspace is given and whole tiles would not divide evenly.
 Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes) {
   Fp8Plan pl{};
   pl.transposed = (M <= 256);
@@ -204,9 +254,10 @@ Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, 
   int bn = 256;
   if (pl.transposed) {
     bn = 16;
-    while (bn < pl.J) bn *= 2;
+    while (bn < pl.J && bn < 64) bn *= 2;
   }
   pl.bn = bn;
+  pl.ctas_per_sm = (bn <= 64) ? 2 : 1;     // Fp8Cfg<bn>::kCtasPerSm
   pl.kblocks = static_cast<int>((K + kBKBytes - 1) / kBKBytes);
   finish_plan(pl, have_ws_budget, ws_bytes);
   return pl;
@@ -216,7 +267,7 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
   pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
   pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
   const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
-  const int sms = sm_count();
+  const int sms = sm_count() * (pl.ctas_per_sm > 0 ? pl.ctas_per_sm : 1);
   pl.streamk = 0;
   pl.grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   if (have_ws && tiles % sms != 0) {
@@ -235,7 +286,7 @@ size_t plan_ws_bytes(const Fp8Plan& pl) {
 }
 
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
-                               void* ws, cudaStream_t st) {
+                               void* ws, cudaStream_t st, bool b_static) {
   p.I = static_cast<int>(pl.I);
   p.J = static_cast<int>(pl.J);
   p.i_tiles = pl.i_tiles;
@@ -243,6 +294,8 @@ lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const 
   p.kblocks = pl.kblocks;
   p.streamk = pl.streamk;
   p.transposed = pl.transposed;
+  p.j_fast = pl.transposed;
+  p.b_static = b_static ? 1 : 0;
   if (pl.streamk) {
     const int tiles = pl.i_tiles * pl.j_tiles;
     const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;

@@ -19,6 +19,7 @@ struct Fp8Plan {
   int64_t I, J;       // rows of the A / B operands
   int i_tiles, j_tiles, kblocks;
   int streamk;        // 1: equal K-iteration ranges per CTA (needs a workspace)
+  int ctas_per_sm;    // resident CTAs per SM the kernel is built for (grid = SMs x this)
   int grid;
 };
 
@@ -29,7 +30,7 @@ size_t plan_ws_bytes(const Fp8Plan& pl);
 // fill in tile counts / stream-K choice / grid for the given tiling
 void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
-                               void* ws, cudaStream_t st);
+                               void* ws, cudaStream_t st, bool b_static = false);
 
 lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
                             const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();      // inputs of this call may come from the previous kernel
+  pdl_launch();
   const int tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {
@@ -218,8 +220,7 @@ lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int6
   p.ldy = ldy;
   p.err = error_word_ptr();
   const int grid = std::min(p.m_tiles * p.n_tiles, sm_count());
-  gemm_fp8_block_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, p);
-  return after_launch();
+  return launch_pdl(gemm_fp8_block_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmA, tmB, p);
 }
 
 }  // namespace lpq

@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   __syncthreads();
+  pdl_wait();      // inputs of this call may come from the previous kernel
+  pdl_launch();
   const int tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {
@@ -207,8 +209,7 @@ lpq_status launch_int8(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M
   p.ldy = ldy;
   p.err = error_word_ptr();
   const int grid = std::min(p.m_tiles * p.n_tiles, sm_count());
-  gemm_int8_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, p);
-  return after_launch();
+  return launch_pdl(gemm_int8_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmA, tmB, p);
 }
 
 }  // namespace lpq

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 
 #include "../../include/lpq.h"
 
@@ -19,6 +20,27 @@ int sm_count();
 // Check the result of a kernel launch (cudaGetLastError) and count it.
 inline lpq_status after_launch() {
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda(e);
+  count_launch();
+  return LPQ_OK;
+}
+
+// Launch a kernel with programmatic stream serialization (the kernel calls
+// pdl_wait() before touching global memory), then check and count it.
+template <typename... KArgs, typename... Args>
+inline lpq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   if (e != cudaSuccess) return record_cuda(e);
   count_launch();
   return LPQ_OK;

@@ -24,6 +24,15 @@ __device__ __forceinline__ uint32_t lane_id() {
   return l;
 }
 
+// ------------------------------------------------- programmatic launch ----
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the previous kernel on the stream is
+// still running.  pdl_wait() blocks until that kernel has finished and its
+// memory is visible, so each thread calls it before its first access to
+// global memory; pdl_launch() then lets the next kernel begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -129,6 +129,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kRowThreads) quant_row_kernel(const uint16_t* __restrict__ X, int64_t K,
                                                                  int64_t ldx, const float* __restrict__ smooth,
                                                                  uint8_t* __restrict__ Q, float* __restrict__ S) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const uint16_t* xr = X + row * ldx;
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(kRowThreads) quant_row_kernel(const uint16_t* 
 __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t* __restrict__ X, int64_t M,
                                                                  int64_t K, int64_t ldx, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
+  pdl_wait();
+  pdl_launch();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t chunks_per_row = K / 8;
   const int64_t total = M * chunks_per_row;
@@ -214,6 +218,8 @@ __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t*
 __global__ void __launch_bounds__(256) quant_fp8_block128_kernel(const uint16_t* __restrict__ W, int64_t N,
                                                                  int64_t K, int64_t ldw, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[8];
   const int64_t nb = blockIdx.y, kb = blockIdx.x;
   const int col8 = threadIdx.x & 15;
@@ -249,6 +255,8 @@ __global__ void __launch_bounds__(256) quant_fp8_block128_kernel(const uint16_t*
 __global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                                int64_t ldx, const float* __restrict__ S,
                                                                uint8_t* __restrict__ Q) {
+  pdl_wait();
+  pdl_launch();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t cpr = K / 8;
   if (t >= M * cpr) return;
@@ -267,6 +275,8 @@ __global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* _
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                           int64_t ldx, float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[8];
   const int64_t cpr = K / 8;
   const int64_t total = M * cpr;
@@ -297,6 +307,8 @@ __device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t kb4) {
 __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                           int64_t ldx, uint8_t* __restrict__ Q,
                                                           uint8_t* __restrict__ SF, float* __restrict__ gs) {
+  pdl_wait();
+  pdl_launch();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t cpr = K / 8;
   const int64_t total = M * cpr;
@@ -348,6 +360,8 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __rest
 __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                           int64_t ldx, uint8_t* __restrict__ Q,
                                                           uint8_t* __restrict__ SF) {
+  pdl_wait();
+  pdl_launch();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t cpr = K / 8;
   const int64_t total = M * cpr;
@@ -391,6 +405,8 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __rest
 // Zero the padding of a scale-factor buffer: rows [rows, rows_pad) of every
 // tile and blocks [kblocks, kb4*4) of every row.
 __global__ void sf_pad_kernel(uint8_t* __restrict__ SF, int64_t rows, int64_t kblocks) {
+  pdl_wait();
+  pdl_launch();
   const int64_t kb4 = (kblocks + 3) / 4;
   const int64_t rows_pad = (rows + 127) / 128 * 128;
   const int64_t n = rows_pad * kb4 * 4;
@@ -416,12 +432,11 @@ lpq_status launch_row(int mode, const uint16_t* X, int64_t M, int64_t K, int64_t
   if (M > 0x7FFFFFFFLL) return LPQ_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(M));
   switch (mode) {
-    case 0: quant_row_kernel<0><<<grid, kRowThreads, 0, st>>>(X, K, ldx, smooth, Q, S); break;
-    case 1: quant_row_kernel<1><<<grid, kRowThreads, 0, st>>>(X, K, ldx, smooth, Q, S); break;
-    case 2: quant_row_kernel<2><<<grid, kRowThreads, 0, st>>>(X, K, ldx, smooth, Q, S); break;
-    default: quant_row_kernel<3><<<grid, kRowThreads, 0, st>>>(X, K, ldx, smooth, Q, S); break;
+    case 0: return launch_pdl(quant_row_kernel<0>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
+    case 1: return launch_pdl(quant_row_kernel<1>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
+    case 2: return launch_pdl(quant_row_kernel<2>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
+    default: return launch_pdl(quant_row_kernel<3>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
   }
-  return after_launch();
 }
 
 lpq_status fp4_common(bool nv, const uint16_t* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Q, uint8_t* SF,
@@ -439,20 +454,22 @@ lpq_status fp4_common(bool nv, const uint16_t* X, int64_t M, int64_t K, int64_t 
     if (e != cudaSuccess) return record_cuda(e);
     const int64_t total = M * (K / 8);
     const int64_t blocks = std::min<int64_t>(grid_for(total), static_cast<int64_t>(sm_count()) * 8);
-    tensor_amax_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, M, K, ldx, gs);
-    if ((s = after_launch()) != LPQ_OK) return s;
-    quant_nvfp4_kernel<<<static_cast<unsigned>(grid_for(total)), 256, 0, st>>>(X, M, K, ldx, Q, SF, gs);
-    if ((s = after_launch()) != LPQ_OK) return s;
+    if ((s = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, X, M, K, ldx,
+                        gs)) != LPQ_OK)
+      return s;
+    if ((s = launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M, K,
+                        ldx, Q, SF, gs)) != LPQ_OK)
+      return s;
   } else {
     const int64_t total = M * (K / 8);
-    quant_mxfp4_kernel<<<static_cast<unsigned>(grid_for(total)), 256, 0, st>>>(X, M, K, ldx, Q, SF);
-    if ((s = after_launch()) != LPQ_OK) return s;
+    if ((s = launch_pdl(quant_mxfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M, K,
+                        ldx, Q, SF)) != LPQ_OK)
+      return s;
   }
   const int64_t kblocks = K / (nv ? 16 : 32);
   if (M % 128 != 0 || kblocks % 4 != 0) {
-    sf_pad_kernel<<<static_cast<unsigned>(std::min<int64_t>(grid_for((M + 127) / 128 * 128 * (kblocks + 3)), 4096)),
-                    256, 0, st>>>(SF, M, kblocks);
-    if ((s = after_launch()) != LPQ_OK) return s;
+    const unsigned pg = static_cast<unsigned>(std::min<int64_t>(grid_for((M + 127) / 128 * 128 * (kblocks + 3)), 4096));
+    if ((s = launch_pdl(sf_pad_kernel, dim3(pg), dim3(256), 0, st, SF, M, kblocks)) != LPQ_OK) return s;
   }
   return LPQ_OK;
 }
@@ -479,13 +496,13 @@ lpq_status lpq_quantize_act_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t
       return launch_row(0, X, M, K, ldx, nullptr, Xq, sx, st);
     case LPQ_GRAN_BLOCK_1x128: {
       const int64_t total = M * (K / 8);
-      quant_fp8_group128_kernel<<<static_cast<unsigned>(grid_for(total)), 256, 0, st>>>(X, M, K, ldx, Xq, sx);
-      return after_launch();
+      return launch_pdl(quant_fp8_group128_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M,
+                        K, ldx, Xq, sx);
     }
     case LPQ_GRAN_TENSOR_STATIC: {
       const int64_t total = M * (K / 8);
-      quant_fp8_static_kernel<<<static_cast<unsigned>(grid_for(total)), 256, 0, st>>>(X, M, K, ldx, sx, Xq);
-      return after_launch();
+      return launch_pdl(quant_fp8_static_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M,
+                        K, ldx, static_cast<const float*>(sx), Xq);
     }
     default:
       return LPQ_ERR_UNSUPPORTED;
@@ -505,8 +522,7 @@ lpq_status lpq_quantize_weight_fp8(const uint16_t* W, int64_t N, int64_t K, int6
   if (g == LPQ_GRAN_ROW) return launch_row(0, W, N, K, ldw, nullptr, Wq, sw, st);
   if (g == LPQ_GRAN_BLOCK_128x128) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    quant_fp8_block128_kernel<<<grid, 256, 0, st>>>(W, N, K, ldw, Wq, sw);
-    return after_launch();
+    return launch_pdl(quant_fp8_block128_kernel, grid, dim3(256), 0, st, W, N, K, ldw, Wq, sw);
   }
   return LPQ_ERR_UNSUPPORTED;
 }

@@ -20,6 +20,8 @@ namespace {
 __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restrict__ X, int64_t rows, int64_t K,
                                                          int64_t ld, int64_t rows_per_slice,
                                                          unsigned int* __restrict__ out) {
+  pdl_wait();
+  pdl_launch();
   const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c8 * 8 >= K) return;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_slice;
@@ -38,6 +40,8 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restr
 
 // s_j from ax_j and aw_j (aw held in s on entry), fp64 power, one rounding.
 __global__ void smooth_finalize_kernel(const float* __restrict__ ax, float* __restrict__ s, int64_t K, float alpha) {
+  pdl_wait();
+  pdl_launch();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= K) return;
   const double a = static_cast<double>(alpha);
@@ -54,9 +58,8 @@ lpq_status launch_colmax(const uint16_t* X, int64_t rows, int64_t K, int64_t ld,
   slices = std::min<int64_t>(slices, 65535);
   const int64_t per = (rows + slices - 1) / slices;
   slices = (rows + per - 1) / per;
-  col_absmax_kernel<<<dim3(gx, static_cast<unsigned>(slices)), 256, 0, st>>>(X, rows, K, ld, per,
-                                                                             reinterpret_cast<unsigned int*>(out));
-  return after_launch();
+  return launch_pdl(col_absmax_kernel, dim3(gx, static_cast<unsigned>(slices)), dim3(256), 0, st, X, rows, K, ld, per,
+                    reinterpret_cast<unsigned int*>(out));
 }
 
 }  // namespace
@@ -92,8 +95,8 @@ lpq_status lpq_smooth_calibrate(const float* chan_amax, const uint16_t* W, int64
   if (e != cudaSuccess) return record_cuda(e);
   lpq_status r = launch_colmax(W, N, K, ldw, s, st);
   if (r != LPQ_OK) return r;
-  smooth_finalize_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, st>>>(chan_amax, s, K, alpha);
-  return after_launch();
+  return launch_pdl(smooth_finalize_kernel, dim3(static_cast<unsigned>((K + 255) / 256)), dim3(256), 0, st, chan_amax, s,
+                    K, alpha);
 }
 
 }  // extern "C"

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(HERE, "liblpq.so")
 LPQ_OK, LPQ_ERR_NULL, LPQ_ERR_SHAPE, LPQ_ERR_ALIGN, LPQ_ERR_UNSUPPORTED, LPQ_ERR_CUDA, LPQ_ERR_WORKSPACE = range(7)
 GRAN_ROW, GRAN_BLOCK_1x128, GRAN_BLOCK_128x128, GRAN_TENSOR_STATIC = range(4)
 FMT_FP8, FMT_INT8, FMT_NVFP4, FMT_MXFP4 = range(4)
+GEMM_B_STATIC = 1
 
 EXPORTS = (
     "lpq_status_string", "lpq_last_cuda_error", "lpq_read_error_word", "lpq_clear_error_word",
@@ -52,6 +53,7 @@ class GemmDesc(ctypes.Structure):
         ("ga", c_void_p), ("gb", c_void_p),
         ("Y", c_void_p), ("ldy", c_int64),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("flags", c_uint32),
     ]
 
 
@@ -192,7 +194,7 @@ def lpq_sf_offset(fmt, rows, K, r, kb):
 
 
 def make_desc(fmt, a_gran, b_gran, A, B, sa, sb, Y, *, M, N, K, lda=None, ldb=None, ga=None, gb=None,
-              workspace=None):
+              workspace=None, flags=0):
     d = GemmDesc()
     d.fmt, d.a_gran, d.b_gran = int(fmt), int(a_gran), int(b_gran)
     d.M, d.N, d.K = int(M), int(N), int(K)
@@ -206,6 +208,7 @@ def make_desc(fmt, a_gran, b_gran, A, B, sa, sb, Y, *, M, N, K, lda=None, ldb=No
     d.Y, d.ldy = Y.data_ptr(), int(Y.stride(0))
     if workspace is not None:
         d.workspace, d.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    d.flags = int(flags)
     return d
 
 
@@ -301,10 +304,11 @@ def smooth_calibrate(chan_amax, W, alpha=0.5, stream=None):
 
 
 def gemm_scaled(fmt, a_gran, b_gran, A, B, sa, sb, *, M, N, K, ga=None, gb=None, workspace=None, Y=None,
-                stream=None):
+                stream=None, flags=0):
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    d = make_desc(fmt, a_gran, b_gran, A, B, sa, sb, Y, M=M, N=N, K=K, ga=ga, gb=gb, workspace=workspace)
+    d = make_desc(fmt, a_gran, b_gran, A, B, sa, sb, Y, M=M, N=N, K=K, ga=ga, gb=gb, workspace=workspace,
+                  flags=flags)
     lpq_gemm_scaled(d, stream)
     return Y
 
