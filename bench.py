@@ -275,7 +275,7 @@ def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
             sx = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             desc = L.make_desc(L.FMT_FP8, L.GRAN_BLOCK_1x128, L.GRAN_BLOCK_128x128, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
-            W.keep = getattr(W, "keep", []) + [desc]
+            W.keep = getattr(W, "keep", []) + [desc, Wq, sw, Xq, sx, Y]
             W.calls.append(dict(kind="quant_fp8_1x128", M=M, K=K, N=N,
                                 fn=(lambda Xd=Xd, Xq=Xq, sx=sx: L.lpq_quantize_act_fp8(Xd, L.GRAN_BLOCK_1x128, Xq, sx)),
                                 bytes=M * K * 3 + 4 * M * K // 128, flops=0))
@@ -319,7 +319,7 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
             sx = torch.empty((M,), dtype=torch.float32, device="cuda")
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             desc = L.make_desc(L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
-            W.keep = getattr(W, "keep", []) + [desc]
+            W.keep = getattr(W, "keep", []) + [desc, Wq, sw, sm, Xq, sx, Y]
             W.calls.append(dict(kind="quant_int8_smooth", M=M, K=K, N=N,
                                 fn=(lambda Xd=Xd, Xq=Xq, sx=sx, sm=sm: L.lpq_quantize_act_int8(Xd, sm, Xq, sx)),
                                 bytes=M * K * 3 + 4 * M, flops=0))

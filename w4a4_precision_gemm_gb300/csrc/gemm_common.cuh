@@ -42,34 +42,38 @@ struct Seg {
   int g_first, n_contrib, slot;
 };
 
-// Iterates the pieces of CTA `g` of `G`.  Data-parallel mode: tiles g, g+G,
-// ...  Stream-K mode: the contiguous range [g T / G, (g+1) T / G) of the
-// T = tiles x kblocks (tile-major) K iterations, cut at tile boundaries.
+// Iterates the pieces of CTA `g` of `G`.  Whole tiles are dealt round-robin
+// in waves of G (tiles g, g+G, ...: at any moment the CTAs work on G
+// consecutive tiles, which share operand rows in L2).  In stream-K mode only
+// the full waves are dealt that way; the K iterations of the leftover tiles
+// (T = leftover tiles x kblocks, tile-major) are split into G equal,
+// contiguous ranges [g T / G, (g+1) T / G), cut at tile boundaries.
 struct WorkIter {
-  int64_t it, end;
-  int tile_rr;
+  int tile_rr, dp_tiles;
+  int64_t it, end, T;
   __device__ __forceinline__ WorkIter(const GemmParams& p, int g, int G) {
-    const int64_t T = static_cast<int64_t>(p.i_tiles) * p.j_tiles * p.kblocks;
+    const int tiles = p.i_tiles * p.j_tiles;
+    dp_tiles = p.streamk ? (tiles / G) * G : tiles;
+    tile_rr = g;
+    T = static_cast<int64_t>(tiles - dp_tiles) * p.kblocks;
     it = p.streamk ? (static_cast<int64_t>(g) * T) / G : 0;
     end = p.streamk ? (static_cast<int64_t>(g + 1) * T) / G : 0;
-    tile_rr = g;
   }
-  // CTA whose range holds iteration x: the largest g with floor(g T / G) <= x
+  // CTA whose range holds leftover iteration x: the largest g with floor(g T / G) <= x
   __device__ __forceinline__ static int owner(int64_t x, int64_t T, int G) {
     return static_cast<int>(((x + 1) * G - 1) / T);
   }
   __device__ __forceinline__ bool next(const GemmParams& p, int g, int G, Seg& s) {
-    const int tiles = p.i_tiles * p.j_tiles;
-    if (!p.streamk) {
-      if (tile_rr >= tiles) return false;
+    if (tile_rr < dp_tiles) {
       s.tile = tile_rr;
       tile_rr += G;
       s.kb0 = 0;
       s.kb1 = p.kblocks;
     } else {
       if (it >= end) return false;
-      s.tile = static_cast<int>(it / p.kblocks);
-      s.kb0 = static_cast<int>(it - static_cast<int64_t>(s.tile) * p.kblocks);
+      const int t = static_cast<int>(it / p.kblocks);
+      s.tile = dp_tiles + t;
+      s.kb0 = static_cast<int>(it - static_cast<int64_t>(t) * p.kblocks);
       const int64_t left = end - it;
       s.kb1 = static_cast<int>(s.kb0 + left < p.kblocks ? s.kb0 + left : p.kblocks);
       it += s.kb1 - s.kb0;
@@ -86,8 +90,7 @@ struct WorkIter {
     s.n_contrib = 1;
     s.slot = 0;
     if (!s.full) {
-      const int64_t T = static_cast<int64_t>(tiles) * p.kblocks;
-      const int64_t a = static_cast<int64_t>(s.tile) * p.kblocks;
+      const int64_t a = static_cast<int64_t>(s.tile - dp_tiles) * p.kblocks;
       s.g_first = owner(a, T, G);
       s.n_contrib = owner(a + p.kblocks - 1, T, G) - s.g_first + 1;
       // the first contributor's piece is the last of its range (slot 1); every

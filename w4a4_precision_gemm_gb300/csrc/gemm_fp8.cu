@@ -267,13 +267,16 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
   pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
   pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
   const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
-  const int sms = sm_count() * (pl.ctas_per_sm > 0 ? pl.ctas_per_sm : 1);
+  const int slots = sm_count() * (pl.ctas_per_sm > 0 ? pl.ctas_per_sm : 1);
   pl.streamk = 0;
-  pl.grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-  if (have_ws && tiles % sms != 0) {
+  pl.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
+  if (have_ws && tiles % slots != 0) {
+    // full waves of whole tiles, then the leftover tiles' K iterations
+    // spread over every CTA
     Fp8Plan sk = pl;
     sk.streamk = 1;
-    sk.grid = static_cast<int>(std::min<int64_t>(tiles * pl.kblocks, sms));
+    const int64_t left_iters = (tiles % slots) * pl.kblocks;
+    sk.grid = static_cast<int>(tiles >= slots ? slots : std::min<int64_t>(left_iters, slots));
     if (plan_ws_bytes(sk) <= ws_bytes) pl = sk;
   }
 }

@@ -209,6 +209,8 @@ def make_desc(fmt, a_gran, b_gran, A, B, sa, sb, Y, *, M, N, K, lda=None, ldb=No
     if workspace is not None:
         d.workspace, d.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     d.flags = int(flags)
+    # the descriptor holds raw device pointers: keep the tensors alive with it
+    d._tensors = (A, B, sa, sb, ga, gb, Y, workspace)
     return d
 
 
