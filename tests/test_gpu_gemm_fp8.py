@@ -61,11 +61,13 @@ def test_fp8_rowscale_gemm(M, N, K, workspace):
 
 
 def test_fp8_workspace_counters_return_to_zero():
+    """A prefill-shaped problem with few tiles uses stream-K partial sums in
+    the workspace; after every call the tile counters are back at zero."""
     L = lpq()
-    M, N, K = 1, 4096, 4096
+    M, N, K = 300, 512, 4096
     _, _, qx, sx, qw, sw = _oracle_operands(M, N, K, 77)
     ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
-    assert ws.numel() > 16, "expected a split-K plan for a single-token 4096x4096 GEMM"
+    assert ws.numel() > 16, "expected a stream-K plan for 6 tiles"
     yr, b = _ref(qx, sx, qw, sw)
     for _ in range(3):
         A, B = dev(qx), dev(qw)
@@ -73,7 +75,7 @@ def test_fp8_workspace_counters_return_to_zero():
         torch.cuda.synchronize()
         ok, worst = G.check(bf16_to_f64(host(Y)), yr, b)
         assert ok.all(), worst
-    tiles = (N + 127) // 128
+    tiles = ((M + 127) // 128) * ((N + 255) // 256)
     counters = host(ws)[: tiles * 4 * 4].view(np.int32)
     assert not counters.any()
     assert L.lpq_read_error_word() == 0

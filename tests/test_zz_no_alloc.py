@@ -40,8 +40,10 @@ def _problem(M, N, K, seed):
 def test_noalloc_matches_gemm_scaled_on_two_calls():
     L = lpq()
     f = _noalloc(L)
-    # two different problems back to back: the shared scratch is reused
-    for (M, N, K, seed) in ((16, 4096, 4096, 11), (1, 6144, 4096, 12)):
+    # different problems back to back: the first needs the built-in scratch
+    # (more than 256 tokens and few tiles: stream-K partial sums), so the
+    # shared array is written, and reused by the second
+    for (M, N, K, seed) in ((300, 256, 512, 13), (300, 512, 1024, 14), (16, 4096, 4096, 11), (1, 6144, 4096, 12)):
         A, sa, B, sb, absum = _problem(M, N, K, seed)
         Y_ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)

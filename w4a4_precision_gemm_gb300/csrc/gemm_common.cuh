@@ -20,6 +20,8 @@ struct GemmParams {
   int i_tiles, j_tiles;        // tiles of 128 rows of A, BN rows of B
   int kblocks;                 // K blocks (one pipeline stage each)
   int streamk;                 // 0: whole tiles round-robin; 1: equal K-iteration ranges per CTA
+  int csplit;                  // > 1: cluster split-K, one (tile, K slice) per CTA, csplit CTAs per cluster
+  int kb_per_split;            // K blocks per cluster rank
   int b_static;                // weights not written by the previous kernel: may be read before its end
   int j_fast;                  // tile order: 1 = consecutive tiles share the A rows (i), 0 = share B rows (j)
   int transposed;              // 0: Y[i][j], 1: Y[j][i]
@@ -64,6 +66,28 @@ struct WorkIter {
     return static_cast<int>(((x + 1) * G - 1) / T);
   }
   __device__ __forceinline__ bool next(const GemmParams& p, int g, int G, Seg& s) {
+    if (p.csplit > 1) {
+      // one piece per CTA: rank r of the cluster takes the r-th K slice of
+      // tile g / csplit; the slices are summed through shared memory
+      if (tile_rr < 0) return false;
+      const int rank = g % p.csplit;
+      s.tile = g / p.csplit;
+      s.kb0 = rank * p.kb_per_split;
+      s.kb1 = min(p.kblocks, s.kb0 + p.kb_per_split);
+      tile_rr = -1;
+      if (p.j_fast) {
+        s.j_tile = s.tile % p.j_tiles;
+        s.i_tile = s.tile / p.j_tiles;
+      } else {
+        s.i_tile = s.tile % p.i_tiles;
+        s.j_tile = s.tile / p.i_tiles;
+      }
+      s.full = false;
+      s.g_first = g - rank;
+      s.n_contrib = p.csplit;
+      s.slot = rank;
+      return true;
+    }
     if (tile_rr < dp_tiles) {
       s.tile = tile_rr;
       tile_rr += G;
@@ -133,9 +157,13 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j
         const float swb = p.sw ? __ldg(p.sw + static_cast<int64_t>(j0 + c + 1) * p.sw_stride) : 1.0f;
         w[c / 2] = pack_bf16x2(scale_one(p, v[c], sxi, swa, g), scale_one(p, v[c + 1], sxi, swb, g));
       }
+      if constexpr (N == 4) {
+        *reinterpret_cast<uint2*>(yrow + j0) = make_uint2(w[0], w[1]);
+      } else {
 #pragma unroll
-      for (int c = 0; c < N / 2; c += 4)
-        *reinterpret_cast<uint4*>(yrow + j0 + 2 * c) = make_uint4(w[c], w[c + 1], w[c + 2], w[c + 3]);
+        for (int c = 0; c < N / 2; c += 4)
+          *reinterpret_cast<uint4*>(yrow + j0 + 2 * c) = make_uint4(w[c], w[c + 1], w[c + 2], w[c + 3]);
+      }
     } else {
 #pragma unroll
       for (int c = 0; c < N; ++c) {
@@ -165,15 +193,17 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j
 // slot of the workspace.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w, uint32_t tmem_acc, int quarter,
-                                              int lane) {
+                                              int lane, float* smem_part = nullptr) {
   constexpr int CW = (BN < 32) ? BN : 32;
   const int row_in_tile = quarter * 32 + lane;
   const int i = w.i_tile * 128 + row_in_tile;
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
   // partial slot layout [BN/4][128][4]: for one group of 4 columns the 32
-  // lanes of a warp touch 512 contiguous bytes
+  // lanes of a warp touch 512 contiguous bytes (global stream-K slot, or this
+  // CTA's shared-memory buffer for a cluster split)
   float* part = w.full ? nullptr
-                       : p.ws + (static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 * BN + row_in_tile * 4;
+                : smem_part ? smem_part + row_in_tile * 4
+                            : p.ws + (static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 * BN + row_in_tile * 4;
 #pragma unroll 1
   for (int c = 0; c < BN; c += CW) {
     float v[CW];
@@ -192,6 +222,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
     }
     if (w.full) {
       epilogue_store<CW>(p, i, w.j_tile * BN + c, v);
+    } else if (smem_part) {
+#pragma unroll
+      for (int t = 0; t < CW; t += 4)
+        *reinterpret_cast<float4*>(part + ((c + t) / 4) * 512) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
     } else {
 #pragma unroll
       for (int t = 0; t < CW; t += 4)
@@ -250,6 +284,29 @@ __device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w
       }
     }
     epilogue_store<kSub>(p, i, w.j_tile * BN + c, v);
+  }
+}
+
+// Cluster split-K: after every CTA of the cluster has put its partial tile
+// (layout [BN/4][128][4] fp32) in its own shared memory and the cluster has
+// synchronised, CTA `rank` sums 1/csplit of the tile's float4 groups over all
+// ranks in rank order (a fixed order) through distributed shared memory and
+// stores them.  Run by the 128 epilogue threads (t = 0..127).
+template <int BN>
+__device__ __forceinline__ void cluster_reduce_store(const GemmParams& p, const Seg& w, uint32_t part_saddr, int t) {
+  constexpr int F = 32 * BN;                    // float4 groups in the tile
+  const int S = p.csplit;
+  const int rank = w.slot;
+  const int q0 = (rank * F) / S, q1 = ((rank + 1) * F) / S;
+  for (int q = q0 + t; q < q1; q += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < S; ++r) {
+      const float4 v = ld_dsmem_f4(map_to_rank(part_saddr + q * 16, static_cast<uint32_t>(r)));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int c4 = q / 128, row = q % 128;
+    const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+    epilogue_store<4>(p, w.i_tile * 128 + row, w.j_tile * BN + 4 * c4, v4);
   }
 }
 

@@ -236,7 +236,7 @@ lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const ui
   static uint64_t done_mask = 0;
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp4_kernel<BN, NV>), C::kSmemBytes, &done_mask);
   if (s != LPQ_OK) return s;
-  return launch_pdl(gemm_fp4_kernel<BN, NV>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, tmA, tmB, sfa, sfb, kb4,
+  return launch_pdl(gemm_fp4_kernel<BN, NV>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, 1, tmA, tmB, sfa, sfb, kb4,
                     p);
 }
 

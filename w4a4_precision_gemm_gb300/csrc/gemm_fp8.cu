@@ -213,13 +213,31 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
     while (wi.next(p, blockIdx.x, gridDim.x, w)) {
       if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x104u, abort_flag)) break;
       tc_fence_after();
-      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
+      // a cluster split's partial goes to this CTA's (now idle) stage buffers
+      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane,
+                        p.csplit > 1 ? reinterpret_cast<float*>(sA) : nullptr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (!w.full) streamk_finish<BN>(p, w, quarter, lane);
+      if (!w.full && p.csplit <= 1) streamk_finish<BN>(p, w, quarter, lane);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+  }
+
+  if (p.csplit > 1) {
+    // every thread of the cluster takes part in both cluster barriers (also
+    // after a timed-out wait), so no CTA can be left waiting at one; the warp
+    // is reconverged first (the TMA and MMA lanes leave their loops later)
+    __syncwarp();
+    cluster_sync();                       // all partials written
+    if (warp >= 2) {
+      WorkIter wi(p, blockIdx.x, gridDim.x);
+      Seg w;
+      if (wi.next(p, blockIdx.x, gridDim.x, w))
+        cluster_reduce_store<BN>(p, w, smem_u32(sA), threadIdx.x - 64);
+    }
+    __syncwarp();
+    cluster_sync();                       // peers done reading this CTA's partial
   }
 
   tc_fence_before();
@@ -229,13 +247,57 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
 }
 
 template <int BN>
-lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, cudaStream_t st) {
+lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, cudaStream_t st,
+                     int cluster) {
   using C = Fp8Cfg<BN>;
   static uint64_t done_mask = 0;
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes,
                                   &done_mask);
   if (s != LPQ_OK) return s;
-  return launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, tmA, tmB, p);
+  return launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, cluster, tmA, tmB, p);
+}
+
+// Clusters of `S` CTAs of the BN kernel that can be resident at once
+// (cached per device, BN and S).
+template <int BN>
+int max_active_clusters_bn(int S) {
+  using C = Fp8Cfg<BN>;
+  static int cache[64][9] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || S < 1 || S > 8) return 0;
+  if (cache[dev][S] != 0) return cache[dev][S] > 0 ? cache[dev][S] : 0;
+  static uint64_t done_mask = 0;
+  int n = 0;
+  if (ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes, &done_mask) ==
+      LPQ_OK) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_rowscale_kernel<BN>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  cache[dev][S] = n > 0 ? n : -1;
+  return n;
+}
+
+int max_active_clusters(int bn, int S) {
+  switch (bn) {
+    case 16: return max_active_clusters_bn<16>(S);
+    case 32: return max_active_clusters_bn<32>(S);
+    case 64: return max_active_clusters_bn<64>(S);
+    default: return 0;
+  }
 }
 
 }  // namespace
@@ -259,6 +321,30 @@ Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, 
   pl.bn = bn;
   pl.ctas_per_sm = (bn <= 64) ? 2 : 1;     // Fp8Cfg<bn>::kCtasPerSm
   pl.kblocks = static_cast<int>((K + kBKBytes - 1) / kBKBytes);
+  if (pl.transposed) {
+    // decode: whole tiles when they fill at least half of the CTA slots;
+    // fewer tiles are split along K across a thread-block cluster whose
+    // CTAs add their partial sums through distributed shared memory
+    pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
+    pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
+    const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
+    const int slots = sm_count() * pl.ctas_per_sm;
+    pl.streamk = 0;
+    pl.csplit = 1;
+    pl.kb_per_split = pl.kblocks;
+    if (tiles * 2 <= slots && pl.kblocks >= 2) {
+      // the widest split (<= 8) whose clusters all fit on the GPU at once
+      for (int S = static_cast<int>(std::min<int64_t>({8, slots / tiles, pl.kblocks})); S >= 2; --S) {
+        const int fit = max_active_clusters(pl.bn, S);
+        if (fit > 0 && tiles > fit) continue;   // (0: unknown, no device) -> take it
+        pl.kb_per_split = (pl.kblocks + S - 1) / S;
+        pl.csplit = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;   // no empty slice
+        break;
+      }
+    }
+    pl.grid = static_cast<int>(pl.csplit > 1 ? tiles * pl.csplit : std::min<int64_t>(tiles, slots));
+    return pl;
+  }
   finish_plan(pl, have_ws_budget, ws_bytes);
   return pl;
 }
@@ -268,6 +354,8 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
   pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
   const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
   const int slots = sm_count() * (pl.ctas_per_sm > 0 ? pl.ctas_per_sm : 1);
+  pl.csplit = 1;
+  pl.kb_per_split = pl.kblocks;
   pl.streamk = 0;
   pl.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
   if (have_ws && tiles % slots != 0) {
@@ -298,6 +386,8 @@ lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const 
   p.streamk = pl.streamk;
   p.transposed = pl.transposed;
   p.j_fast = pl.transposed;
+  p.csplit = pl.csplit;
+  p.kb_per_split = pl.kb_per_split;
   p.b_static = b_static ? 1 : 0;
   if (pl.streamk) {
     const int tiles = pl.i_tiles * pl.j_tiles;
@@ -306,11 +396,11 @@ lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const 
     p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
   }
   switch (pl.bn) {
-    case 16: return launch_bn<16>(tmA, tmB, p, pl.grid, st);
-    case 32: return launch_bn<32>(tmA, tmB, p, pl.grid, st);
-    case 64: return launch_bn<64>(tmA, tmB, p, pl.grid, st);
-    case 128: return launch_bn<128>(tmA, tmB, p, pl.grid, st);
-    case 256: return launch_bn<256>(tmA, tmB, p, pl.grid, st);
+    case 16: return launch_bn<16>(tmA, tmB, p, pl.grid, st, pl.csplit);
+    case 32: return launch_bn<32>(tmA, tmB, p, pl.grid, st, pl.csplit);
+    case 64: return launch_bn<64>(tmA, tmB, p, pl.grid, st, pl.csplit);
+    case 128: return launch_bn<128>(tmA, tmB, p, pl.grid, st, pl.csplit);
+    case 256: return launch_bn<256>(tmA, tmB, p, pl.grid, st, pl.csplit);
     default: return LPQ_ERR_UNSUPPORTED;
   }
 }

@@ -20,6 +20,8 @@ struct Fp8Plan {
   int i_tiles, j_tiles, kblocks;
   int streamk;        // 1: equal K-iteration ranges per CTA (needs a workspace)
   int ctas_per_sm;    // resident CTAs per SM the kernel is built for (grid = SMs x this)
+  int csplit;         // > 1: K split across a cluster of this many CTAs (one tile per cluster)
+  int kb_per_split;   // K blocks per cluster rank
   int grid;
 };
 

@@ -220,7 +220,7 @@ lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int6
   p.ldy = ldy;
   p.err = error_word_ptr();
   const int grid = std::min(p.m_tiles * p.n_tiles, sm_count());
-  return launch_pdl(gemm_fp8_block_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmA, tmB, p);
+  return launch_pdl(gemm_fp8_block_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, 1, tmA, tmB, p);
 }
 
 }  // namespace lpq

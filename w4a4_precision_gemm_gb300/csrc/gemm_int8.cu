@@ -209,7 +209,7 @@ lpq_status launch_int8(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M
   p.ldy = ldy;
   p.err = error_word_ptr();
   const int grid = std::min(p.m_tiles * p.n_tiles, sm_count());
-  return launch_pdl(gemm_int8_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmA, tmB, p);
+  return launch_pdl(gemm_int8_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, 1, tmA, tmB, p);
 }
 
 }  // namespace lpq

@@ -432,10 +432,10 @@ lpq_status launch_row(int mode, const uint16_t* X, int64_t M, int64_t K, int64_t
   if (M > 0x7FFFFFFFLL) return LPQ_ERR_SHAPE;
   dim3 grid(static_cast<unsigned>(M));
   switch (mode) {
-    case 0: return launch_pdl(quant_row_kernel<0>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
-    case 1: return launch_pdl(quant_row_kernel<1>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
-    case 2: return launch_pdl(quant_row_kernel<2>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
-    default: return launch_pdl(quant_row_kernel<3>, grid, dim3(kRowThreads), 0, st, X, K, ldx, smooth, Q, S);
+    case 0: return launch_pdl(quant_row_kernel<0>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
+    case 1: return launch_pdl(quant_row_kernel<1>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
+    case 2: return launch_pdl(quant_row_kernel<2>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
+    default: return launch_pdl(quant_row_kernel<3>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
   }
 }
 
@@ -454,22 +454,22 @@ lpq_status fp4_common(bool nv, const uint16_t* X, int64_t M, int64_t K, int64_t 
     if (e != cudaSuccess) return record_cuda(e);
     const int64_t total = M * (K / 8);
     const int64_t blocks = std::min<int64_t>(grid_for(total), static_cast<int64_t>(sm_count()) * 8);
-    if ((s = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, X, M, K, ldx,
+    if ((s = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, X, M, K, ldx,
                         gs)) != LPQ_OK)
       return s;
-    if ((s = launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M, K,
+    if ((s = launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M, K,
                         ldx, Q, SF, gs)) != LPQ_OK)
       return s;
   } else {
     const int64_t total = M * (K / 8);
-    if ((s = launch_pdl(quant_mxfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M, K,
+    if ((s = launch_pdl(quant_mxfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M, K,
                         ldx, Q, SF)) != LPQ_OK)
       return s;
   }
   const int64_t kblocks = K / (nv ? 16 : 32);
   if (M % 128 != 0 || kblocks % 4 != 0) {
     const unsigned pg = static_cast<unsigned>(std::min<int64_t>(grid_for((M + 127) / 128 * 128 * (kblocks + 3)), 4096));
-    if ((s = launch_pdl(sf_pad_kernel, dim3(pg), dim3(256), 0, st, SF, M, kblocks)) != LPQ_OK) return s;
+    if ((s = launch_pdl(sf_pad_kernel, dim3(pg), dim3(256), 0, st, 1, SF, M, kblocks)) != LPQ_OK) return s;
   }
   return LPQ_OK;
 }
@@ -496,12 +496,12 @@ lpq_status lpq_quantize_act_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t
       return launch_row(0, X, M, K, ldx, nullptr, Xq, sx, st);
     case LPQ_GRAN_BLOCK_1x128: {
       const int64_t total = M * (K / 8);
-      return launch_pdl(quant_fp8_group128_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M,
+      return launch_pdl(quant_fp8_group128_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M,
                         K, ldx, Xq, sx);
     }
     case LPQ_GRAN_TENSOR_STATIC: {
       const int64_t total = M * (K / 8);
-      return launch_pdl(quant_fp8_static_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, X, M,
+      return launch_pdl(quant_fp8_static_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M,
                         K, ldx, static_cast<const float*>(sx), Xq);
     }
     default:
@@ -522,7 +522,7 @@ lpq_status lpq_quantize_weight_fp8(const uint16_t* W, int64_t N, int64_t K, int6
   if (g == LPQ_GRAN_ROW) return launch_row(0, W, N, K, ldw, nullptr, Wq, sw, st);
   if (g == LPQ_GRAN_BLOCK_128x128) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    return launch_pdl(quant_fp8_block128_kernel, grid, dim3(256), 0, st, W, N, K, ldw, Wq, sw);
+    return launch_pdl(quant_fp8_block128_kernel, grid, dim3(256), 0, st, 1, W, N, K, ldw, Wq, sw);
   }
   return LPQ_ERR_UNSUPPORTED;
 }

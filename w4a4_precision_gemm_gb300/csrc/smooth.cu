@@ -58,7 +58,7 @@ lpq_status launch_colmax(const uint16_t* X, int64_t rows, int64_t K, int64_t ld,
   slices = std::min<int64_t>(slices, 65535);
   const int64_t per = (rows + slices - 1) / slices;
   slices = (rows + per - 1) / per;
-  return launch_pdl(col_absmax_kernel, dim3(gx, static_cast<unsigned>(slices)), dim3(256), 0, st, X, rows, K, ld, per,
+  return launch_pdl(col_absmax_kernel, dim3(gx, static_cast<unsigned>(slices)), dim3(256), 0, st, 1, X, rows, K, ld, per,
                     reinterpret_cast<unsigned int*>(out));
 }
 
@@ -95,7 +95,7 @@ lpq_status lpq_smooth_calibrate(const float* chan_amax, const uint16_t* W, int64
   if (e != cudaSuccess) return record_cuda(e);
   lpq_status r = launch_colmax(W, N, K, ldw, s, st);
   if (r != LPQ_OK) return r;
-  return launch_pdl(smooth_finalize_kernel, dim3(static_cast<unsigned>((K + 255) / 256)), dim3(256), 0, st, chan_amax, s,
+  return launch_pdl(smooth_finalize_kernel, dim3(static_cast<unsigned>((K + 255) / 256)), dim3(256), 0, st, 1, chan_amax, s,
                     K, alpha);
 }
 
