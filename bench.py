@@ -121,6 +121,62 @@ def measure_int8_library_peak(torch, n=8192, reps=10):
     return 2.0 * n ** 3 / (best * 1e-3) / 1e12
 
 
+# --------------------------------------------------------------- traffic --
+TRAFFIC_FILES = {"gemm_fp8": "gemm_fp8_decode_traffic.txt", "gemm_fp4": "gemm_fp4_nvfp4_traffic.txt",
+                 "gemm_fp8_block": "gemm_fp8_block_prefill_traffic.txt", "gemm_int8": "gemm_int8_traffic.txt"}
+KERNEL_SOURCES = {"gemm_fp8": ["gemm_fp8.cu", "gemm_common.cuh", "ptx.cuh"],
+                  "gemm_fp4": ["gemm_fp4.cu", "gemm_common.cuh", "ptx.cuh"],
+                  "gemm_fp8_block": ["gemm_fp8_block.cu", "gemm_common.cuh", "ptx.cuh"],
+                  "gemm_int8": ["gemm_int8.cu", "gemm_common.cuh", "ptx.cuh"]}
+
+
+def kernel_source_hash(kind: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kind, []):
+        with open(os.path.join(ROOT, "w4a4_precision_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str):
+    """DRAM bytes per launch of `kind` from the committed ncu summary, or
+    None when there is none or the kernel's sources changed since it was taken."""
+    name = TRAFFIC_FILES.get(kind)
+    path = os.path.join(ROOT, "profiles", name) if name else None
+    if not path or not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != kernel_source_hash(kind):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------- multi-process --
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of `x` over all ranks (the job is as slow as its
+    slowest replica); `x` itself without a process group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Work of all replicas per second (weak scaling: every rank runs the
+    same step on its own GPU)."""
+    return work_per_rank_step * world / (ms_per_step * 1e-3)
+
+
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
@@ -578,14 +634,11 @@ def main():
     ms_dom = timed(g_dom, dom_steps)
     timed(g_ins, lambda: ins_steps(stream, external=False))
     clocks = clk.stop()
-    if dist:
-        tt = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dist, "cuda")
     ms_step = ms_total / args.steps
 
     flops_step = sum(c["flops"] for c in W.calls)
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    value = whole_job_rate(flops_step, world, ms_step) / 1e12
 
     # per-kernel statistics from the instrumented replay
     kinds = {}
@@ -623,7 +676,7 @@ def main():
     roofline = {"bound": W.dominant_bound, "kernel": W.dominant, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak,
                 "peak_src": peak_src,
-                "traffic": None,
+                "traffic": recorded_traffic(W.dominant),
                 "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"],
                 "algorithmic_flops_per_launch": dom["flops"] / dom["launches"],
                 "avg_launch_us": 1000 * ms_dom / dom["launches"],
@@ -656,8 +709,8 @@ def main():
         e2e_steps()
     e_e.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e) / n_e2e
-    e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / n_e2e, dist, "cuda")
+    e2e_val = whole_job_rate(flops_step, world, e2e_ms) / 1e12
     GE.close()
 
     cpu = None

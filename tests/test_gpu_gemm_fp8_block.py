@@ -37,10 +37,10 @@ def test_fp8_block_gemm(M, N, K):
     Y = L.gemm_scaled(L.FMT_FP8, L.GRAN_BLOCK_1x128, L.GRAN_BLOCK_128x128, dev(qx), dev(qw),
                       dev(np.ascontiguousarray(sx.T)), dev(sw), M=M, N=N, K=K)
     torch.cuda.synchronize()
+    assert L.lpq_read_error_word() == 0
     yr, b = G.matmul_ref(*_dequant_block(qx, sx, qw, sw))
     ok, worst = G.check(bf16_to_f64(host(Y)), yr, b)
     assert ok.all(), f"{(~ok).sum()} of {ok.size} out of tolerance, worst {worst:.3g}"
-    assert L.lpq_read_error_word() == 0
 
 
 def test_fp8_block_end_to_end():
@@ -53,6 +53,7 @@ def test_fp8_block_end_to_end():
     qw, sw = L.quantize_weight_fp8(dev_bf16(wb), L.GRAN_BLOCK_128x128)
     Y = L.gemm_scaled(L.FMT_FP8, L.GRAN_BLOCK_1x128, L.GRAN_BLOCK_128x128, qx, qw, sx, sw, M=M, N=N, K=K)
     torch.cuda.synchronize()
+    assert L.lpq_read_error_word() == 0
     qxo, sxo = Q.fp8_per_group_1x128(synth.f32_from_bf16_bits(xb))
     qwo, swo = Q.fp8_per_block_128x128_ragged(synth.f32_from_bf16_bits(wb))
     yr, b = G.matmul_ref(*_dequant_block(qxo, sxo, qwo, swo))

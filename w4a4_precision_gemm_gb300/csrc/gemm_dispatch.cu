@@ -70,7 +70,7 @@ lpq_status gemm_fp8_block(const lpq_gemm_desc* d, cudaStream_t st) {
   LPQ_CHECK_NULL(d->sb);
   CUtensorMap tmA, tmB;
   if ((s = make_tmap_u8(&tmA, d->A, d->M, d->K, d->lda, 128, 128, true)) != LPQ_OK) return s;
-  if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K, d->ldb, 128, 128, true)) != LPQ_OK) return s;
+  if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K, d->ldb, 128, kFp8BlockBN, true)) != LPQ_OK) return s;
   return launch_fp8_block(tmA, tmB, d->M, d->N, d->K, static_cast<const float*>(d->sa),
                           static_cast<const float*>(d->sb), d->Y, d->ldy, st);
 }

@@ -333,10 +333,13 @@ Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, 
     pl.csplit = 1;
     pl.kb_per_split = pl.kblocks;
     if (tiles * 2 <= slots && pl.kblocks >= 2) {
-      // the widest split (<= 8) whose clusters all fit on the GPU at once
-      for (int S = static_cast<int>(std::min<int64_t>({8, slots / tiles, pl.kblocks})); S >= 2; --S) {
+      // the widest power-of-two split (8, 4 or 2: they pack evenly into the
+      // GPCs) that keeps tiles x split within the CTA slots and whose clusters
+      // fit on the GPU in at most two waves
+      for (int S = 8; S >= 2; S /= 2) {
+        if (tiles * S > slots || S > pl.kblocks) continue;
         const int fit = max_active_clusters(pl.bn, S);
-        if (fit > 0 && tiles > fit) continue;   // (0: unknown, no device) -> take it
+        if (fit > 0 && tiles > 2 * fit) continue;   // (0: unknown / no device)
         pl.kb_per_split = (pl.kblocks + S - 1) / S;
         pl.csplit = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;   // no empty slice
         break;

@@ -34,6 +34,8 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st, bool b_static = false);
 
+// Output tile width of the block-scaled FP8 kernel (two 128-column weight blocks).
+constexpr int kFp8BlockBN = 256;
 lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
                             const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
 

@@ -11,7 +11,7 @@
 // Warp roles as in the row-scaled kernel, except that the tensor-memory
 // buffers hold per-group partial sums (NP of them, so the MMA of group kb+1..
 // overlaps the promotion of group kb) and the running accumulator lives in
-// the epilogue threads' registers (thread = output row, 128 columns).
+// the epilogue threads' registers (thread = output row, 128 of 256 columns).
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -24,14 +24,15 @@
 namespace lpq {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // two per tensor-memory lane quarter, 128 columns each
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBN = kFp8BlockBN;
 constexpr int kBK = 128;
-constexpr int kNP = 4;                       // partial-sum buffers in tensor memory
+constexpr int kNP = 2;                       // partial-sum buffers in tensor memory
 constexpr int kStageBytes = (kBM + kBN) * kBK;
-constexpr int kStages = 6;
-constexpr int kTmemCols = 512;               // kNP x 128
+constexpr int kStages = 4;
+constexpr int kTmemCols = 512;               // kNP x 256
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 
@@ -45,7 +46,9 @@ struct BlockParams {
   uint32_t* err;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// 10 warps put three on some SM sub-partitions, whose register file holds
+// 16K registers, so 168 per thread is the most this block can launch with.
+__global__ void __maxnreg__(168)
     gemm_fp8_block_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const BlockParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNP; ++b) {
       mbar_init(pfull(b), 1);
-      mbar_init(pempty(b), 4);
+      mbar_init(pempty(b), kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -146,9 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, nullptr, 0, &no_abort);
     }
   } else {
-    // epilogue / promotion: thread = one output row, all 128 columns
-    const int quarter = warp & 3;
+    // epilogue / promotion: thread = one output row, 128 of the 256 columns
+    // (one 128-column weight block, so one weight scale per K group)
+    const int quarter = warp & 3;             // lane quarter this warp may read
+    const int half = (warp - 2) / 4;          // column half of the tile
     const int row_in_tile = quarter * 32 + lane;
+    const int nb_count = (p.N + 127) / 128;
     uint32_t pb = 0, pphase = 0;
     bool ok = true;
     GemmParams ep{};
@@ -160,18 +166,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = t % p.m_tiles, nt = t / p.m_tiles;
       const int m = mt * kBM + row_in_tile;
       const bool row_ok = m < p.M;
-      float acc[kBN];
+      const int nb = nt * 2 + half;
+      const bool nb_ok = nb < nb_count;
+      float acc[128];
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < p.kblocks; ++kb) {
         const float sxv = row_ok ? __ldg(p.sx + static_cast<int64_t>(kb) * p.M + m) : 0.0f;
-        const float swv = __ldg(p.sw + static_cast<int64_t>(nt) * p.kblocks + kb);
+        const float swv = nb_ok ? __ldg(p.sw + static_cast<int64_t>(nb) * p.kblocks + kb) : 0.0f;
         const float c = __fmul_rn(sxv, swv);
         if (!mbar_wait(pfull(pb), pphase, p.err, 0x304u, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + pb * kBN + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t taddr = tmem_base + pb * kBN + half * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c0, r);
           tmem_ld_wait();
@@ -185,11 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = acc[c0 + j];
-        epilogue_store<32>(ep, m, nt * kBN + c0, v);
+        epilogue_store<32>(ep, m, nt * kBN + half * 128 + c0, v);
       }
     }
   }
@@ -207,6 +215,14 @@ lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int6
   static uint64_t done_mask = 0;
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_block_kernel), kSmemBytes, &done_mask);
   if (s != LPQ_OK) return s;
+  static int max_threads = 0;
+  if (max_threads == 0) {
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&gemm_fp8_block_kernel));
+    if (e != cudaSuccess) return record_cuda(e);
+    max_threads = fa.maxThreadsPerBlock;
+  }
+  if (max_threads < kThreads) return record_cuda(cudaErrorLaunchOutOfResources);
   BlockParams p{};
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
