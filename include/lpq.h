@@ -42,7 +42,7 @@ extern "C" {
 typedef enum {
   LPQ_OK = 0,
   LPQ_ERR_NULL = 1,         /* a required pointer is NULL                          */
-  LPQ_ERR_SHAPE = 2,        /* a size is <= 0, K not a multiple of the block, ld < K */
+  LPQ_ERR_SHAPE = 2,        /* a size is <= 0, K not a multiple of the block, ld < K; quantizers: M or N >= 2^31, K > 2^30 */
   LPQ_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned / ld not a multiple of 8 */
   LPQ_ERR_UNSUPPORTED = 4,  /* format / granularity combination not provided        */
   LPQ_ERR_CUDA = 5,         /* a launch failed; see lpq_last_cuda_error()          */

@@ -42,6 +42,10 @@ struct Seg {
   int tile, i_tile, j_tile, kb0, kb1;
   bool full;
   int g_first, n_contrib, slot;
+  // stream-K pieces: the tile's first leftover iteration and the leftover
+  // iteration count; with fewer leftover iterations than CTAs some CTAs own
+  // none, so contributor s of the tile is the owner of iteration sk_a + s
+  int64_t sk_a, sk_T;
 };
 
 // Iterates the pieces of CTA `g` of `G`.  Whole tiles are dealt round-robin
@@ -116,7 +120,12 @@ struct WorkIter {
     if (!s.full) {
       const int64_t a = static_cast<int64_t>(s.tile - dp_tiles) * p.kblocks;
       s.g_first = owner(a, T, G);
-      s.n_contrib = owner(a + p.kblocks - 1, T, G) - s.g_first + 1;
+      s.sk_a = a;
+      s.sk_T = T;
+      // T >= G: every CTA owns at least one iteration, so the contributors
+      // are consecutive; T < G: every CTA owns at most one, so there is one
+      // contributor per iteration of the tile
+      s.n_contrib = (T >= G) ? owner(a + p.kblocks - 1, T, G) - s.g_first + 1 : p.kblocks;
       // the first contributor's piece is the last of its range (slot 1); every
       // later contributor's piece is the first of its range (slot 0)
       s.slot = (g == s.g_first) ? 1 : 0;
@@ -267,7 +276,8 @@ __device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         if (s0 + b < w.n_contrib) {
-          const int g = w.g_first + s0 + b;
+          const int G = static_cast<int>(gridDim.x);
+          const int g = (w.sk_T >= G) ? w.g_first + s0 + b : WorkIter::owner(w.sk_a + s0 + b, w.sk_T, G);
           const int slot = (s0 + b == 0) ? 1 : 0;
           const float* part = p.ws + (static_cast<int64_t>(g) * 2 + slot) * 128 * BN + row_off +
                               static_cast<int64_t>(c / 4) * 512;

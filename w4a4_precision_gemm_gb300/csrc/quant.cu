@@ -22,7 +22,6 @@ namespace {
 
 constexpr float kScaleFloor = 1e-8f;   // clamp(min=1e-8) of the per-token scale
 constexpr int kRowThreads = 256;       // threads per row in the per-row kernels
-constexpr int kRowMaxChunks = 8;       // 8-element chunks per thread kept in registers
 
 struct Chunk8 {
   float v[8];
@@ -93,9 +92,34 @@ __device__ __forceinline__ uint32_t int8_code(float v) {
 }
 
 // ------------------------------------------------------------------------
-// Per-row quantizers: one CTA of 256 threads per row.  The row stays in
-// registers between the max pass and the code pass when K <= 256*8*8; longer
-// rows are read a second time (from L2).
+// Memory-level parallelism.  Each thread issues kCPT independent 16-byte
+// loads before it uses any of them, so a resident thread keeps 64 bytes in
+// flight; register use stays low enough for full occupancy.
+// ------------------------------------------------------------------------
+constexpr int kCPT = 4;
+
+__device__ __forceinline__ void zero8(Chunk8& c) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c.v[i] = 0.0f;
+}
+
+// Block-wide max for any blockDim that is a multiple of 32 (<= 1024).
+__device__ __forceinline__ float block_max_any(float v, float* red) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < nw; ++i) r = fmaxf(r, red[i]);
+  __syncthreads();
+  return r;
+}
+
+// ------------------------------------------------------------------------
+// Per-row quantizers: one CTA per row, blockDim chosen on the host so that
+// the row fits in kCPT chunks per thread (registers) up to 1024 threads;
+// longer rows are read a second time (from L2).
 // MODE 0: FP8 (x / s), MODE 1: INT8 activation (x / smooth_j), MODE 2: INT8
 // weight (w * smooth_j), MODE 3: INT8 without smoothing.
 // ------------------------------------------------------------------------
@@ -126,49 +150,54 @@ __device__ __forceinline__ void emit_codes(const Chunk8& c, float s, uint8_t* ou
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kRowThreads) quant_row_kernel(const uint16_t* __restrict__ X, int64_t K,
-                                                                 int64_t ldx, const float* __restrict__ smooth,
-                                                                 uint8_t* __restrict__ Q, float* __restrict__ S) {
+__global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t* __restrict__ X, int K, int64_t ldx,
+                                                          const float* __restrict__ smooth, uint8_t* __restrict__ Q,
+                                                          float* __restrict__ S) {
   pdl_wait();
   pdl_launch();
-  __shared__ float red[kRowThreads / 32];
+  __shared__ float red[32];
   const int64_t row = blockIdx.x;
   const uint16_t* xr = X + row * ldx;
   uint8_t* qr = Q + row * K;
-  const int nchunks = static_cast<int>(K / 8);
+  const int T = blockDim.x;
+  const int nchunks = K / 8;
   const float qmax = (MODE == 0) ? 448.0f : 127.0f;
-
-  if (nchunks <= kRowThreads * kRowMaxChunks) {
-    Chunk8 c[kRowMaxChunks];
+  if (nchunks <= T * kCPT) {
+    Chunk8 c[kCPT];
+#pragma unroll
+    for (int j = 0; j < kCPT; ++j) {
+      const int ci = j * T + threadIdx.x;
+      if (ci < nchunks) c[j] = load_bf16x8_stream(xr + static_cast<int64_t>(ci) * 8);
+      else zero8(c[j]);
+    }
     float a = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kRowMaxChunks; ++j) {
-      const int ci = j * kRowThreads + threadIdx.x;
+    for (int j = 0; j < kCPT; ++j) {
+      const int ci = j * T + threadIdx.x;
       if (ci < nchunks) {
-        c[j] = load_bf16x8_stream(xr + static_cast<int64_t>(ci) * 8);
         pre_transform<MODE>(c[j], smooth, static_cast<int64_t>(ci) * 8);
         a = fmaxf(a, amax8(c[j]));
       }
     }
-    a = block_max(a, red);
+    a = block_max_any(a, red);
     const float s = __fdiv_rn(fmaxf(a, kScaleFloor), qmax);
     if (threadIdx.x == 0) S[row] = s;
 #pragma unroll
-    for (int j = 0; j < kRowMaxChunks; ++j) {
-      const int ci = j * kRowThreads + threadIdx.x;
+    for (int j = 0; j < kCPT; ++j) {
+      const int ci = j * T + threadIdx.x;
       if (ci < nchunks) emit_codes<MODE>(c[j], s, qr + static_cast<int64_t>(ci) * 8);
     }
   } else {
     float a = 0.0f;
-    for (int ci = threadIdx.x; ci < nchunks; ci += kRowThreads) {
+    for (int ci = threadIdx.x; ci < nchunks; ci += T) {
       Chunk8 c = load_bf16x8(xr + static_cast<int64_t>(ci) * 8);
       pre_transform<MODE>(c, smooth, static_cast<int64_t>(ci) * 8);
       a = fmaxf(a, amax8(c));
     }
-    a = block_max(a, red);
+    a = block_max_any(a, red);
     const float s = __fdiv_rn(fmaxf(a, kScaleFloor), qmax);
     if (threadIdx.x == 0) S[row] = s;
-    for (int ci = threadIdx.x; ci < nchunks; ci += kRowThreads) {
+    for (int ci = threadIdx.x; ci < nchunks; ci += T) {
       Chunk8 c = load_bf16x8(xr + static_cast<int64_t>(ci) * 8);
       pre_transform<MODE>(c, smooth, static_cast<int64_t>(ci) * 8);
       emit_codes<MODE>(c, s, qr + static_cast<int64_t>(ci) * 8);
@@ -177,38 +206,43 @@ __global__ void __launch_bounds__(kRowThreads) quant_row_kernel(const uint16_t* 
 }
 
 // ------------------------------------------------------------------------
-// FP8 per 1x128 group: 16 threads per group (8 elements each); the scale is
-// stored K-group major: S[kg * M + row].
+// FP8 per 1x128 group.  Grid (ceil(M/64), K/128): a CTA covers 64 rows of one
+// K group; a warp covers 8 rows, two per pass (half-warp = one 128-element
+// group, 8 elements per lane).  The scale is stored K-group major,
+// S[kg * M + row], so consecutive rows give consecutive scale stores.
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t* __restrict__ X, int64_t M,
                                                                  int64_t K, int64_t ldx, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
   pdl_wait();
   pdl_launch();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t chunks_per_row = K / 8;
-  const int64_t total = M * chunks_per_row;
-  // Threads past the end still take part in the shuffles (with zeros).
-  const bool live = t < total;
-  const int64_t row = live ? t / chunks_per_row : 0;
-  const int64_t c8 = live ? t % chunks_per_row : 0;
-  Chunk8 c;
-  if (live) {
-    c = load_bf16x8_stream(X + row * ldx + c8 * 8);
-  } else {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t kg = blockIdx.y;
+  const int sub = lane & 15;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64 + warp * 8 + (lane >> 4);
+  const int64_t col = kg * 128 + sub * 8;
+  Chunk8 c[kCPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c.v[i] = 0.0f;
+  for (int j = 0; j < kCPT; ++j) {
+    const int64_t row = r0 + 2 * j;
+    if (row < M) c[j] = load_bf16x8_stream(X + row * ldx + col);
+    else zero8(c[j]);
   }
-  float a = amax8(c);
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float s = __fdiv_rn(fmaxf(a, kScaleFloor), 448.0f);
-  if (!live) return;
-  if ((c8 & 15) == 0) S[(c8 >> 4) * M + row] = s;
-  float q[8];
+  for (int j = 0; j < kCPT; ++j) {
+    const int64_t row = r0 + 2 * j;
+    float a = amax8(c[j]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c.v[i], s);
-  *reinterpret_cast<uint2*>(Q + row * K + c8 * 8) = e4m3x8(q);
+    for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float s = __fdiv_rn(fmaxf(a, kScaleFloor), 448.0f);
+    if (row < M) {
+      if (sub == 0) S[kg * M + row] = s;
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c[j].v[i], s);
+      *reinterpret_cast<uint2*>(Q + row * K + col) = e4m3x8(q);
+    }
+  }
 }
 
 // ------------------------------------------------------------------------
@@ -250,50 +284,68 @@ __global__ void __launch_bounds__(256) quant_fp8_block128_kernel(const uint16_t*
 }
 
 // ------------------------------------------------------------------------
-// FP8 with a given (static) per-tensor scale: q = E4M3(x / s).
+// Row-segment mapping shared by the elementwise and block-16/32 kernels:
+// grid (rows, segments), blockDim T (multiple of 32); thread t of segment y
+// handles chunks y*T*kCPT + j*T + t, j < kCPT, of its row.  Lanes of a warp
+// hold consecutive chunks for each j.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
+__device__ __forceinline__ int seg_chunk(int j) {
+  return static_cast<int>(blockIdx.y) * static_cast<int>(blockDim.x) * kCPT + j * static_cast<int>(blockDim.x) +
+         static_cast<int>(threadIdx.x);
+}
+
+// FP8 with a given (static) per-tensor scale: q = E4M3(x / s).
+__global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* __restrict__ X, int64_t K,
                                                                int64_t ldx, const float* __restrict__ S,
                                                                uint8_t* __restrict__ Q) {
   pdl_wait();
   pdl_launch();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t cpr = K / 8;
-  if (t >= M * cpr) return;
-  const int64_t row = t / cpr, c8 = t % cpr;
+  const int64_t row = blockIdx.x;
+  const int cpr = static_cast<int>(K / 8);
   const float s = __ldg(S);
-  Chunk8 c = load_bf16x8_stream(X + row * ldx + c8 * 8);
-  float q[8];
+  Chunk8 c[kCPT];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c.v[i], s);
-  *reinterpret_cast<uint2*>(Q + row * K + c8 * 8) = e4m3x8(q);
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    if (c8 < cpr) c[j] = load_bf16x8_stream(X + row * ldx + static_cast<int64_t>(c8) * 8);
+  }
+#pragma unroll
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    if (c8 < cpr) {
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c[j].v[i], s);
+      *reinterpret_cast<uint2*>(Q + row * K + static_cast<int64_t>(c8) * 8) = e4m3x8(q);
+    }
+  }
 }
 
 // ------------------------------------------------------------------------
-// Tensor max|x| (NVFP4 pass 1): grid-stride, block reduce, one atomicMax of
-// the fp32 bit pattern (non-negative floats order like their bits).
+// Tensor max|x| (NVFP4 pass 1): CTAs stride over rows with the row-segment
+// mapping, block reduce, one atomicMax of the fp32 bit pattern (non-negative
+// floats order like their bits).
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                           int64_t ldx, float* __restrict__ out) {
   pdl_wait();
   pdl_launch();
-  __shared__ float red[8];
-  const int64_t cpr = K / 8;
-  const int64_t total = M * cpr;
+  __shared__ float red[32];
+  const int cpr = static_cast<int>(K / 8);
   float a = 0.0f;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = t / cpr, c8 = t % cpr;
-    a = fmaxf(a, amax8(load_bf16x8(X + row * ldx + c8 * 8)));
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    Chunk8 c[kCPT];
+#pragma unroll
+    for (int j = 0; j < kCPT; ++j) {
+      const int c8 = seg_chunk(j);
+      if (c8 < cpr) c[j] = load_bf16x8(X + row * ldx + static_cast<int64_t>(c8) * 8);
+      else zero8(c[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kCPT; ++j) a = fmaxf(a, amax8(c[j]));
   }
-  a = warp_max(a);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float r = red[0];
-    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[i]);
-    atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(r));
-  }
+  a = block_max_any(a, red);
+  if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(a));
 }
 
 // Offset of scale (r, kb) in the 128x4-tile layout of lpq_sf_offset.
@@ -302,103 +354,106 @@ __device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t kb4) {
 }
 
 // ------------------------------------------------------------------------
-// NVFP4 pass 2: two threads per 16-element block.
+// NVFP4 pass 2 (row-segment mapping): two lanes per 16-element block; eight
+// lanes = four consecutive blocks = one 32-bit word of scale codes.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
-                                                          int64_t ldx, uint8_t* __restrict__ Q,
-                                                          uint8_t* __restrict__ SF, float* __restrict__ gs) {
+__global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __restrict__ X, int64_t K, int64_t ldx,
+                                                          uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
+                                                          float* __restrict__ gs) {
   pdl_wait();
   pdl_launch();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t cpr = K / 8;
-  const int64_t total = M * cpr;
-  const bool live = t < total;
-  const int64_t row = live ? t / cpr : 0;
-  const int64_t c8 = live ? t % cpr : 0;
+  const int64_t row = blockIdx.x;
+  const int cpr = static_cast<int>(K / 8);
   const float amax = gs[0];
   const float g = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;   // 448 * 6
-  if (t == 0) gs[1] = g;
-  Chunk8 c;
-  if (live) {
-    c = load_bf16x8_stream(X + row * ldx + c8 * 8);
-  } else {
+  if (row == 0 && blockIdx.y == 0 && threadIdx.x == 0) gs[1] = g;
+  Chunk8 c[kCPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c.v[i] = 0.0f;
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    if (c8 < cpr) c[j] = load_bf16x8_stream(X + row * ldx + static_cast<int64_t>(c8) * 8);
+    else zero8(c[j]);
   }
-  float ab = amax8(c);
-  ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
-  const float tsc = __fdiv_rn(__fdiv_rn(ab, 6.0f), g);
-  const uint32_t code = cvt_e4m3x2(tsc, 0.0f) & 0xFFu;
-  uint32_t packed = 0;
-  if (code != 0) {
-    const float s = __fmul_rn(e4m3_to_f32(code), g);
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c.v[i], s);
-    packed = cvt_e2m1x8(q);
-  }
-  // scale codes of 4 consecutive blocks -> one 32-bit word (lanes 8j..8j+7)
   const int lane = threadIdx.x & 31;
-  uint32_t word = code << (8 * ((lane >> 1) & 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 2);
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
-  if (!live) return;
-  *reinterpret_cast<uint32_t*>(Q + row * (K / 2) + c8 * 4) = packed;
-  const int64_t kb = c8 >> 1;
   const int64_t kb4 = ((K / 16) + 3) / 4;
-  if ((K & 63) == 0) {
-    if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(SF + sf_off(row, kb, kb4)) = word;
-  } else if ((c8 & 1) == 0) {
-    SF[sf_off(row, kb, kb4)] = static_cast<uint8_t>(code);
+#pragma unroll
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    float ab = amax8(c[j]);
+    ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
+    const float tsc = __fdiv_rn(__fdiv_rn(ab, 6.0f), g);
+    const uint32_t code = cvt_e4m3x2(tsc, 0.0f) & 0xFFu;
+    uint32_t packed = 0;
+    if (code != 0) {
+      const float s = __fmul_rn(e4m3_to_f32(code), g);
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c[j].v[i], s);
+      packed = cvt_e2m1x8(q);
+    }
+    // scale codes of 4 consecutive blocks -> one 32-bit word (lanes 8i..8i+7)
+    uint32_t word = code << (8 * ((lane >> 1) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    if (c8 < cpr) {
+      *reinterpret_cast<uint32_t*>(Q + row * (K / 2) + static_cast<int64_t>(c8) * 4) = packed;
+      const int64_t kb = c8 >> 1;
+      if ((K & 63) == 0) {
+        if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(SF + sf_off(row, kb, kb4)) = word;
+      } else if ((c8 & 1) == 0) {
+        SF[sf_off(row, kb, kb4)] = static_cast<uint8_t>(code);
+      }
+    }
   }
 }
 
 // ------------------------------------------------------------------------
-// MXFP4: four threads per 32-element block; exponent from the fp32 exponent
-// field of the block max (exact floor(log2)), scaling by an exact power of 2.
+// MXFP4 (row-segment mapping): four lanes per 32-element block; exponent
+// from the fp32 exponent field of the block max (exact floor(log2)), scaling
+// by an exact power of 2.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
-                                                          int64_t ldx, uint8_t* __restrict__ Q,
-                                                          uint8_t* __restrict__ SF) {
+__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t K, int64_t ldx,
+                                                          uint8_t* __restrict__ Q, uint8_t* __restrict__ SF) {
   pdl_wait();
   pdl_launch();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t cpr = K / 8;
-  const int64_t total = M * cpr;
-  const bool live = t < total;
-  const int64_t row = live ? t / cpr : 0;
-  const int64_t c8 = live ? t % cpr : 0;
-  Chunk8 c;
-  if (live) {
-    c = load_bf16x8_stream(X + row * ldx + c8 * 8);
-  } else {
+  const int64_t row = blockIdx.x;
+  const int cpr = static_cast<int>(K / 8);
+  Chunk8 c[kCPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c.v[i] = 0.0f;
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    if (c8 < cpr) c[j] = load_bf16x8_stream(X + row * ldx + static_cast<int64_t>(c8) * 8);
+    else zero8(c[j]);
   }
-  float ab = amax8(c);
-  ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
-  ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
-  const int E = static_cast<int>((__float_as_uint(ab) >> 23) & 0xFFu);
-  // floor(log2 ab) = E - 127 for normal ab; zero / subnormal -> clamp to -127
-  const int e = (E == 0) ? -127 : max(E - 129, -127);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, exact
-  float q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(c.v[i], inv);
-  const uint32_t packed = cvt_e2m1x8(q);
-  const uint32_t code = static_cast<uint32_t>(e + 127);
   const int lane = threadIdx.x & 31;
-  uint32_t word = code << (8 * ((lane >> 2) & 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
-  word |= __shfl_xor_sync(0xffffffffu, word, 8);
-  if (!live) return;
-  *reinterpret_cast<uint32_t*>(Q + row * (K / 2) + c8 * 4) = packed;
-  const int64_t kb = c8 >> 2;
   const int64_t kb4 = ((K / 32) + 3) / 4;
-  if ((K & 127) == 0) {
-    if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(SF + sf_off(row, kb, kb4)) = word;
-  } else if ((c8 & 3) == 0) {
-    SF[sf_off(row, kb, kb4)] = static_cast<uint8_t>(code);
+#pragma unroll
+  for (int j = 0; j < kCPT; ++j) {
+    const int c8 = seg_chunk(j);
+    float ab = amax8(c[j]);
+    ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
+    ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
+    const int E = static_cast<int>((__float_as_uint(ab) >> 23) & 0xFFu);
+    // floor(log2 ab) = E - 127 for normal ab; zero / subnormal -> clamp to -127
+    const int e = (E == 0) ? -127 : max(E - 129, -127);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, exact
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(c[j].v[i], inv);
+    const uint32_t packed = cvt_e2m1x8(q);
+    const uint32_t code = static_cast<uint32_t>(e + 127);
+    uint32_t word = code << (8 * ((lane >> 2) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+    if (c8 < cpr) {
+      *reinterpret_cast<uint32_t*>(Q + row * (K / 2) + static_cast<int64_t>(c8) * 4) = packed;
+      const int64_t kb = c8 >> 2;
+      if ((K & 127) == 0) {
+        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(SF + sf_off(row, kb, kb4)) = word;
+      } else if ((c8 & 3) == 0) {
+        SF[sf_off(row, kb, kb4)] = static_cast<uint8_t>(code);
+      }
+    }
   }
 }
 
@@ -419,23 +474,46 @@ __global__ void sf_pad_kernel(uint8_t* __restrict__ SF, int64_t rows, int64_t kb
 
 int64_t grid_for(int64_t threads, int block = 256) { return (threads + block - 1) / block; }
 
+// Largest row, in elements, that the 32-bit chunk indices of the kernels
+// above cover (K / 8 chunks, times kCPT, in an int).
+constexpr int64_t kMaxK = int64_t(1) << 30;
+
 lpq_status check_x(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, int64_t kmult) {
   LPQ_CHECK_NULL(X);
-  if (M <= 0 || K <= 0 || ldx < K || K % kmult != 0) return LPQ_ERR_SHAPE;
+  if (M <= 0 || K <= 0 || ldx < K || K % kmult != 0 || K > kMaxK || M > 0x7FFFFFFFLL) return LPQ_ERR_SHAPE;
   LPQ_CHECK_ALIGN(X);
   if (ldx % 8 != 0) return LPQ_ERR_ALIGN;
   return LPQ_OK;
 }
 
+// Row-segment launch shape: T threads (multiple of 32, <= 256) and the number
+// of segments per row.
+struct SegShape {
+  int threads;
+  unsigned segs;
+};
+SegShape seg_shape(int64_t K) {
+  const int64_t cpr = K / 8;
+  int64_t t = (cpr + kCPT - 1) / kCPT;
+  t = std::min<int64_t>(256, std::max<int64_t>(32, (t + 31) / 32 * 32));
+  return {static_cast<int>(t), static_cast<unsigned>((cpr + t * kCPT - 1) / (t * kCPT))};
+}
+
 lpq_status launch_row(int mode, const uint16_t* X, int64_t M, int64_t K, int64_t ldx, const float* smooth,
                       uint8_t* Q, float* S, cudaStream_t st) {
-  if (M > 0x7FFFFFFFLL) return LPQ_ERR_SHAPE;
-  dim3 grid(static_cast<unsigned>(M));
+  // Few rows: spread each row over more threads (one chunk each) for latency;
+  // many rows: kCPT chunks per thread for bytes in flight.
+  const int64_t nch = K / 8;
+  const int64_t per = (M < 2 * static_cast<int64_t>(sm_count())) ? 1 : kCPT;
+  int64_t t = (nch + per - 1) / per;
+  t = std::min<int64_t>(1024, std::max<int64_t>(32, (t + 31) / 32 * 32));
+  const dim3 grid(static_cast<unsigned>(M)), block(static_cast<unsigned>(t));
+  const int k = static_cast<int>(K);
   switch (mode) {
-    case 0: return launch_pdl(quant_row_kernel<0>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
-    case 1: return launch_pdl(quant_row_kernel<1>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
-    case 2: return launch_pdl(quant_row_kernel<2>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
-    default: return launch_pdl(quant_row_kernel<3>, grid, dim3(kRowThreads), 0, st, 1, X, K, ldx, smooth, Q, S);
+    case 0: return launch_pdl(quant_row_kernel<0>, grid, block, 0, st, 1, X, k, ldx, smooth, Q, S);
+    case 1: return launch_pdl(quant_row_kernel<1>, grid, block, 0, st, 1, X, k, ldx, smooth, Q, S);
+    case 2: return launch_pdl(quant_row_kernel<2>, grid, block, 0, st, 1, X, k, ldx, smooth, Q, S);
+    default: return launch_pdl(quant_row_kernel<3>, grid, block, 0, st, 1, X, k, ldx, smooth, Q, S);
   }
 }
 
@@ -447,24 +525,20 @@ lpq_status fp4_common(bool nv, const uint16_t* X, int64_t M, int64_t K, int64_t 
   LPQ_CHECK_NULL(SF);
   LPQ_CHECK_ALIGN(Q);
   LPQ_CHECK_ALIGN(SF);
+  const SegShape sh = seg_shape(K);
+  if (sh.segs > 65535u) return LPQ_ERR_SHAPE;
+  const dim3 grid(static_cast<unsigned>(M), sh.segs), block(static_cast<unsigned>(sh.threads));
   if (nv) {
     LPQ_CHECK_NULL(gs);
     if ((reinterpret_cast<uintptr_t>(gs) & 3u) != 0) return LPQ_ERR_ALIGN;
     cudaError_t e = cudaMemsetAsync(gs, 0, sizeof(float), st);
     if (e != cudaSuccess) return record_cuda(e);
-    const int64_t total = M * (K / 8);
-    const int64_t blocks = std::min<int64_t>(grid_for(total), static_cast<int64_t>(sm_count()) * 8);
-    if ((s = launch_pdl(tensor_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, X, M, K, ldx,
-                        gs)) != LPQ_OK)
-      return s;
-    if ((s = launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M, K,
-                        ldx, Q, SF, gs)) != LPQ_OK)
-      return s;
+    const int64_t want = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * (2048 / sh.threads) / sh.segs);
+    const dim3 agrid(static_cast<unsigned>(std::min<int64_t>(M, want)), sh.segs);
+    if ((s = launch_pdl(tensor_amax_kernel, agrid, block, 0, st, 1, X, M, K, ldx, gs)) != LPQ_OK) return s;
+    if ((s = launch_pdl(quant_nvfp4_kernel, grid, block, 0, st, 1, X, K, ldx, Q, SF, gs)) != LPQ_OK) return s;
   } else {
-    const int64_t total = M * (K / 8);
-    if ((s = launch_pdl(quant_mxfp4_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M, K,
-                        ldx, Q, SF)) != LPQ_OK)
-      return s;
+    if ((s = launch_pdl(quant_mxfp4_kernel, grid, block, 0, st, 1, X, K, ldx, Q, SF)) != LPQ_OK) return s;
   }
   const int64_t kblocks = K / (nv ? 16 : 32);
   if (M % 128 != 0 || kblocks % 4 != 0) {
@@ -495,14 +569,16 @@ lpq_status lpq_quantize_act_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t
     case LPQ_GRAN_ROW:
       return launch_row(0, X, M, K, ldx, nullptr, Xq, sx, st);
     case LPQ_GRAN_BLOCK_1x128: {
-      const int64_t total = M * (K / 8);
-      return launch_pdl(quant_fp8_group128_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M,
-                        K, ldx, Xq, sx);
+      if (K / 128 > 65535) return LPQ_ERR_SHAPE;
+      const dim3 grid(static_cast<unsigned>((M + 63) / 64), static_cast<unsigned>(K / 128));
+      return launch_pdl(quant_fp8_group128_kernel, grid, dim3(256), 0, st, 1, X, M, K, ldx, Xq, sx);
     }
     case LPQ_GRAN_TENSOR_STATIC: {
-      const int64_t total = M * (K / 8);
-      return launch_pdl(quant_fp8_static_kernel, dim3(static_cast<unsigned>(grid_for(total))), dim3(256), 0, st, 1, X, M,
-                        K, ldx, static_cast<const float*>(sx), Xq);
+      const SegShape sh = seg_shape(K);
+      if (sh.segs > 65535u) return LPQ_ERR_SHAPE;
+      const dim3 grid(static_cast<unsigned>(M), sh.segs);
+      return launch_pdl(quant_fp8_static_kernel, grid, dim3(static_cast<unsigned>(sh.threads)), 0, st, 1, X, K, ldx,
+                        static_cast<const float*>(sx), Xq);
     }
     default:
       return LPQ_ERR_UNSUPPORTED;
