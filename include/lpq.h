@@ -170,10 +170,12 @@ size_t lpq_sf_offset(lpq_format fmt, int64_t rows, int64_t K, int64_t r, int64_t
  *       point at the tensor scales g (gs + 1); Y = bf16(acc * ga * gb).
  *   fmt MXFP4: as NVFP4 without ga / gb.
  * lda / ldb are row strides in elements (FP4: elements, two per byte).
- * workspace: optional device buffer for stream-K partial sums (tiles shared by two CTAs); if NULL the
- * library picks a tiling that needs none.  Its size for a problem is
- * lpq_gemm_workspace_bytes(desc); it must be zero-filled before its first use
- * and is left zero-filled by every call.  Calls sharing one workspace must be
+ * workspace: optional device buffer for fp32 partial sums: when the output
+ * tiles leave the last wave of CTAs mostly idle, those tiles are split along
+ * K and a second kernel adds the slices in a fixed order.  If NULL (or too
+ * small) the library uses whole tiles only.  Its size for a problem is
+ * lpq_gemm_workspace_bytes(desc) (0 when no split would be used); its
+ * contents need no initialisation.  Calls sharing one workspace must be
  * ordered on one stream.
  * "FP8 and INT8 Inference", sections 5 and 6-9 (the GEMM epilogue);
  * "Low-bit LLM Weights and Activations", section 3.4. */
@@ -210,17 +212,16 @@ lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream);
  *
  * Same operation and arguments as lpq_gemm_scaled for fmt LPQ_FMT_FP8 with
  * a_gran ROW or TENSOR_STATIC and b_gran ROW (other combinations return
- * LPQ_ERR_UNSUPPORTED); d->workspace is ignored.  The stream-K scratch comes
+ * LPQ_ERR_UNSUPPORTED); d->workspace is ignored.  The split-K scratch comes
  * from one array of LPQ_NOALLOC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library holds until the process exits.  A problem whose
- * stream-K scratch would exceed that size returns LPQ_ERR_WORKSPACE and
+ * split-K scratch would exceed that size returns LPQ_ERR_WORKSPACE and
  * enqueues nothing; nothing is allocated or freed.
  * The first call on a device looks up the array's device address (a one-time
  * set-up per device, done with that device current); make that first call
- * before any stream capture.  All calls share the array and it keeps the
- * previous call's contents: the call clears its tile counters itself, but
- * calls that may run at the same time on the GPU race on the array; order
- * them on one stream. */
+ * before any stream capture.  All calls share the array (no call depends on
+ * what an earlier one left in it), so calls that may run at the same time on
+ * the GPU race on it; order them on one stream. */
 #define LPQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream);
 

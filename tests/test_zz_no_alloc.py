@@ -40,10 +40,12 @@ def _problem(M, N, K, seed):
 def test_noalloc_matches_gemm_scaled_on_two_calls():
     L = lpq()
     f = _noalloc(L)
-    # different problems back to back: the first needs the built-in scratch
-    # (more than 256 tokens and few tiles: stream-K partial sums), so the
-    # shared array is written, and reused by the second
-    for (M, N, K, seed) in ((300, 256, 512, 13), (300, 512, 1024, 14), (16, 4096, 4096, 11), (1, 6144, 4096, 12)):
+    # different problems back to back: the first two need the built-in
+    # scratch (153 and 156 output tiles, just over one wave of CTAs: the
+    # leftover tiles are split along K and their partial sums go through the
+    # shared array), the others use a cluster split or whole tiles
+    for (M, N, K, seed) in ((1152, 4352, 256, 13), (256, 19968, 1024, 14), (300, 512, 1024, 15),
+                            (16, 4096, 4096, 11), (1, 6144, 4096, 12)):
         A, sa, B, sb, absum = _problem(M, N, K, seed)
         Y_ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)

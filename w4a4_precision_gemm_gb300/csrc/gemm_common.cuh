@@ -1,6 +1,6 @@
 // gemm_common.cuh - pieces shared by the tcgen05 GEMM kernels: work-unit
-// decoding (data-parallel tiles or stream-K ranges), the scale epilogue and
-// the in-order combination of stream-K partial tiles.
+// decoding (whole tiles in waves, split tail tiles, cluster split-K), the
+// scale epilogue and the in-order combination of partial tiles.
 //
 // Every GEMM here computes D[i, j] = sum_k A[i, k] B[j, k] for a 128-row tile
 // of the "A" operand (the tensor core's M side) and a BN-row tile of the "B"
@@ -9,8 +9,10 @@
 // counts) and the output is written as Y[j][i].
 #pragma once
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cstdint>
 
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace lpq {
@@ -19,9 +21,10 @@ struct GemmParams {
   int I, J, K;                 // rows of A, rows of B, reduction length (elements)
   int i_tiles, j_tiles;        // tiles of 128 rows of A, BN rows of B
   int kblocks;                 // K blocks (one pipeline stage each)
-  int streamk;                 // 0: whole tiles round-robin; 1: equal K-iteration ranges per CTA
+  int dp_tiles;                // tiles dealt whole, round-robin in waves of gridDim.x
+  int tail_s;                  // > 1: the remaining tiles are split into tail_s K slices, one per CTA
   int csplit;                  // > 1: cluster split-K, one (tile, K slice) per CTA, csplit CTAs per cluster
-  int kb_per_split;            // K blocks per cluster rank
+  int kb_per_split;            // K blocks per slice (tail split or cluster rank)
   int b_static;                // weights not written by the previous kernel: may be read before its end
   int j_fast;                  // tile order: 1 = consecutive tiles share the A rows (i), 0 = share B rows (j)
   int transposed;              // 0: Y[i][j], 1: Y[j][i]
@@ -30,44 +33,33 @@ struct GemmParams {
   const float* sw; int sw_stride;
   const float* gx; const float* gw;              // optional extra factors (NVFP4 g)
   uint16_t* Y; int64_t ldy;
-  float* ws;                   // stream-K partials [grid][2][BN/4][128][4]
-  int* counters;               // [tiles * 4], zero on entry, zero on exit
+  float* ws;                   // tail-split partials [tail tiles * tail_s][BN/4][128][4]
   uint32_t* err;
 };
 
 // A piece of work for one CTA: K blocks [kb0, kb1) of one output tile.
-// `full` pieces cover the whole K range; the others are stream-K pieces whose
-// partial sums are combined by the last of the tile's contributors.
+// `full` pieces cover the whole K range; the others are K slices whose
+// partial sums are combined later (by the cluster, or by the tail-reduction
+// kernel); `slot` is the slice's cluster rank or its tail piece index.
 struct Seg {
   int tile, i_tile, j_tile, kb0, kb1;
   bool full;
-  int g_first, n_contrib, slot;
-  // stream-K pieces: the tile's first leftover iteration and the leftover
-  // iteration count; with fewer leftover iterations than CTAs some CTAs own
-  // none, so contributor s of the tile is the owner of iteration sk_a + s
-  int64_t sk_a, sk_T;
+  int slot;
 };
 
 // Iterates the pieces of CTA `g` of `G`.  Whole tiles are dealt round-robin
 // in waves of G (tiles g, g+G, ...: at any moment the CTAs work on G
-// consecutive tiles, which share operand rows in L2).  In stream-K mode only
-// the full waves are dealt that way; the K iterations of the leftover tiles
-// (T = leftover tiles x kblocks, tile-major) are split into G equal,
-// contiguous ranges [g T / G, (g+1) T / G), cut at tile boundaries.
+// consecutive tiles, which share operand rows in L2).  The tiles past
+// dp_tiles (fewer than G) are each cut into tail_s K slices; CTA g takes
+// tail piece g (tile dp_tiles + g / tail_s, slice g % tail_s) after its
+// whole tiles.  With a cluster split every CTA has exactly one piece.
 struct WorkIter {
-  int tile_rr, dp_tiles;
-  int64_t it, end, T;
+  int tile_rr, tail_piece;
   __device__ __forceinline__ WorkIter(const GemmParams& p, int g, int G) {
-    const int tiles = p.i_tiles * p.j_tiles;
-    dp_tiles = p.streamk ? (tiles / G) * G : tiles;
+    (void)G;
     tile_rr = g;
-    T = static_cast<int64_t>(tiles - dp_tiles) * p.kblocks;
-    it = p.streamk ? (static_cast<int64_t>(g) * T) / G : 0;
-    end = p.streamk ? (static_cast<int64_t>(g + 1) * T) / G : 0;
-  }
-  // CTA whose range holds leftover iteration x: the largest g with floor(g T / G) <= x
-  __device__ __forceinline__ static int owner(int64_t x, int64_t T, int G) {
-    return static_cast<int>(((x + 1) * G - 1) / T);
+    const int tail_tiles = p.i_tiles * p.j_tiles - p.dp_tiles;
+    tail_piece = (p.tail_s > 1 && g < tail_tiles * p.tail_s) ? g : -1;
   }
   __device__ __forceinline__ bool next(const GemmParams& p, int g, int G, Seg& s) {
     if (p.csplit > 1) {
@@ -79,32 +71,24 @@ struct WorkIter {
       s.kb0 = rank * p.kb_per_split;
       s.kb1 = min(p.kblocks, s.kb0 + p.kb_per_split);
       tile_rr = -1;
-      if (p.j_fast) {
-        s.j_tile = s.tile % p.j_tiles;
-        s.i_tile = s.tile / p.j_tiles;
-      } else {
-        s.i_tile = s.tile % p.i_tiles;
-        s.j_tile = s.tile / p.i_tiles;
-      }
       s.full = false;
-      s.g_first = g - rank;
-      s.n_contrib = p.csplit;
       s.slot = rank;
-      return true;
-    }
-    if (tile_rr < dp_tiles) {
+    } else if (tile_rr < p.dp_tiles) {
       s.tile = tile_rr;
       tile_rr += G;
       s.kb0 = 0;
       s.kb1 = p.kblocks;
+      s.full = true;
+      s.slot = 0;
+    } else if (tail_piece >= 0) {
+      s.tile = p.dp_tiles + tail_piece / p.tail_s;
+      s.kb0 = (tail_piece % p.tail_s) * p.kb_per_split;
+      s.kb1 = min(p.kblocks, s.kb0 + p.kb_per_split);
+      s.full = false;
+      s.slot = tail_piece;
+      tail_piece = -1;
     } else {
-      if (it >= end) return false;
-      const int t = static_cast<int>(it / p.kblocks);
-      s.tile = dp_tiles + t;
-      s.kb0 = static_cast<int>(it - static_cast<int64_t>(t) * p.kblocks);
-      const int64_t left = end - it;
-      s.kb1 = static_cast<int>(s.kb0 + left < p.kblocks ? s.kb0 + left : p.kblocks);
-      it += s.kb1 - s.kb0;
+      return false;
     }
     if (p.j_fast) {
       s.j_tile = s.tile % p.j_tiles;
@@ -112,23 +96,6 @@ struct WorkIter {
     } else {
       s.i_tile = s.tile % p.i_tiles;
       s.j_tile = s.tile / p.i_tiles;
-    }
-    s.full = (s.kb0 == 0 && s.kb1 == p.kblocks);
-    s.g_first = g;
-    s.n_contrib = 1;
-    s.slot = 0;
-    if (!s.full) {
-      const int64_t a = static_cast<int64_t>(s.tile - dp_tiles) * p.kblocks;
-      s.g_first = owner(a, T, G);
-      s.sk_a = a;
-      s.sk_T = T;
-      // T >= G: every CTA owns at least one iteration, so the contributors
-      // are consecutive; T < G: every CTA owns at most one, so there is one
-      // contributor per iteration of the tile
-      s.n_contrib = (T >= G) ? owner(a + p.kblocks - 1, T, G) - s.g_first + 1 : p.kblocks;
-      // the first contributor's piece is the last of its range (slot 1); every
-      // later contributor's piece is the first of its range (slot 0)
-      s.slot = (g == s.g_first) ? 1 : 0;
     }
     return true;
   }
@@ -198,8 +165,8 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j
 
 // Tensor-memory -> registers -> epilogue for one 128 x BN accumulator, by the
 // four epilogue warps (warp q of the CTA reads lanes 32*(q%4) .. +31).  A full
-// piece is scaled and stored; a stream-K piece writes its partial sums to its
-// slot of the workspace.
+// piece is scaled and stored; a K slice writes its partial sums to its slot
+// (this CTA's shared memory for a cluster split, else the workspace).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w, uint32_t tmem_acc, int quarter,
                                               int lane, float* smem_part = nullptr) {
@@ -208,11 +175,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
   const int i = w.i_tile * 128 + row_in_tile;
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
   // partial slot layout [BN/4][128][4]: for one group of 4 columns the 32
-  // lanes of a warp touch 512 contiguous bytes (global stream-K slot, or this
-  // CTA's shared-memory buffer for a cluster split)
+  // lanes of a warp touch 512 contiguous bytes
   float* part = w.full ? nullptr
                 : smem_part ? smem_part + row_in_tile * 4
-                            : p.ws + (static_cast<int64_t>(blockIdx.x) * 2 + w.slot) * 128 * BN + row_in_tile * 4;
+                            : p.ws + static_cast<int64_t>(w.slot) * 128 * BN + row_in_tile * 4;
 #pragma unroll 1
   for (int c = 0; c < BN; c += CW) {
     float v[CW];
@@ -244,57 +210,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
   }
 }
 
-// Second half of a stream-K piece, run after the accumulator has been handed
-// back to the MMA warp: count this quarter-tile in; the last contributor sums
-// every contributor's partial in contributor order (a fixed order, so the
-// result does not depend on which CTA finishes last) and stores the tile.
+// Tail reduction (its own launch, after the GEMM): sums the tail_s partial
+// tiles of every split tail tile in slice order (a fixed order) and applies
+// the epilogue.  One thread per (tail tile, row, group of 4 columns); the
+// 32 lanes of a warp read 512 contiguous bytes of each slice.
 template <int BN>
-__device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w, int quarter, int lane) {
-  constexpr int kSub = 8;          // columns per reduction step
-  constexpr int kBatch = 8;        // contributors whose loads are in flight together
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) {
-    const int old = atomicAdd(p.counters + w.tile * 4 + quarter, 1);
-    last = (old == w.n_contrib - 1);
-    if (last) p.counters[w.tile * 4 + quarter] = 0;
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const int row_in_tile = quarter * 32 + lane;
-  const int i = w.i_tile * 128 + row_in_tile;
-  const int64_t row_off = static_cast<int64_t>(row_in_tile) * 4;
-#pragma unroll 2
-  for (int c = 0; c < BN; c += kSub) {
-    float v[kSub];
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const GemmParams p) {
+  pdl_wait();
+  pdl_launch();
+  constexpr int kQ = 128 * (BN / 4);            // float4 groups per tile
+  const int tail_tiles = p.i_tiles * p.j_tiles - p.dp_tiles;
+  const int64_t total = static_cast<int64_t>(tail_tiles) * kQ;
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(q / kQ);
+    const int r = static_cast<int>(q % kQ);
+    const int c4 = r / 128, row = r % 128;
+    const float* base = p.ws + static_cast<int64_t>(t) * p.tail_s * 128 * BN + c4 * 512 + row * 4;
+    float4 v[8];
 #pragma unroll
-    for (int t = 0; t < kSub; ++t) v[t] = 0.0f;
-    for (int s0 = 0; s0 < w.n_contrib; s0 += kBatch) {
-      float4 f[kBatch][2];
+    for (int s = 0; s < 8; ++s)
+      if (s < p.tail_s) v[s] = __ldcg(reinterpret_cast<const float4*>(base + static_cast<int64_t>(s) * 128 * BN));
+    float4 acc = v[0];
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        if (s0 + b < w.n_contrib) {
-          const int G = static_cast<int>(gridDim.x);
-          const int g = (w.sk_T >= G) ? w.g_first + s0 + b : WorkIter::owner(w.sk_a + s0 + b, w.sk_T, G);
-          const int slot = (s0 + b == 0) ? 1 : 0;
-          const float* part = p.ws + (static_cast<int64_t>(g) * 2 + slot) * 128 * BN + row_off +
-                              static_cast<int64_t>(c / 4) * 512;
-          f[b][0] = __ldcg(reinterpret_cast<const float4*>(part));
-          f[b][1] = __ldcg(reinterpret_cast<const float4*>(part + 512));
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        if (s0 + b < w.n_contrib) {
-          v[0] += f[b][0].x; v[1] += f[b][0].y; v[2] += f[b][0].z; v[3] += f[b][0].w;
-          v[4] += f[b][1].x; v[5] += f[b][1].y; v[6] += f[b][1].z; v[7] += f[b][1].w;
-        }
+    for (int s = 1; s < 8; ++s) {
+      if (s < p.tail_s) {
+        acc.x += v[s].x; acc.y += v[s].y; acc.z += v[s].z; acc.w += v[s].w;
       }
     }
-    epilogue_store<kSub>(p, i, w.j_tile * BN + c, v);
+    const int tile = p.dp_tiles + t;
+    const int i_tile = p.j_fast ? tile / p.j_tiles : tile % p.i_tiles;
+    const int j_tile = p.j_fast ? tile % p.j_tiles : tile / p.i_tiles;
+    const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+    epilogue_store<4>(p, i_tile * 128 + row, j_tile * BN + 4 * c4, v4);
   }
+}
+
+// Enqueue the tail reduction for a plan with a tail split (after the GEMM on
+// the same stream; programmatic launch lets it wait for the GEMM's end).
+template <int BN>
+lpq_status launch_tail_reduce(const GemmParams& p, cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(p.i_tiles * p.j_tiles - p.dp_tiles) * 128 * (BN / 4);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sm_count()) * 8);
+  return launch_pdl(tail_reduce_kernel<BN>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p);
 }
 
 // Cluster split-K: after every CTA of the cluster has put its partial tile
@@ -305,18 +263,35 @@ __device__ __forceinline__ void streamk_finish(const GemmParams& p, const Seg& w
 template <int BN>
 __device__ __forceinline__ void cluster_reduce_store(const GemmParams& p, const Seg& w, uint32_t part_saddr, int t) {
   constexpr int F = 32 * BN;                    // float4 groups in the tile
-  const int S = p.csplit;
+  constexpr int U = 2;                          // groups per thread per pass
+  const int S = p.csplit;                       // 2 .. 8
   const int rank = w.slot;
   const int q0 = (rank * F) / S, q1 = ((rank + 1) * F) / S;
-  for (int q = q0 + t; q < q1; q += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < S; ++r) {
-      const float4 v = ld_dsmem_f4(map_to_rank(part_saddr + q * 16, static_cast<uint32_t>(r)));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  for (int qb = q0 + t; qb < q1; qb += 128 * U) {
+    // every rank's copy of U groups is requested before any is used
+    float4 v[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = qb + u * 128;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (q < q1 && r < S) v[u][r] = ld_dsmem_f4(map_to_rank(part_saddr + q * 16, static_cast<uint32_t>(r)));
     }
-    const int c4 = q / 128, row = q % 128;
-    const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
-    epilogue_store<4>(p, w.i_tile * 128 + row, w.j_tile * BN + 4 * c4, v4);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = qb + u * 128;
+      if (q >= q1) break;
+      float4 acc = v[u][0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r) {
+        if (r < S) {
+          acc.x += v[u][r].x; acc.y += v[u][r].y; acc.z += v[u][r].z; acc.w += v[u][r].w;
+        }
+      }
+      const int c4 = q / 128, row = q % 128;
+      const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+      epilogue_store<4>(p, w.i_tile * 128 + row, w.j_tile * BN + 4 * c4, v4);
+    }
   }
 }
 

@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (!w.full) streamk_finish<BN>(p, w, quarter, lane);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -236,15 +235,16 @@ lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const ui
   static uint64_t done_mask = 0;
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp4_kernel<BN, NV>), C::kSmemBytes, &done_mask);
   if (s != LPQ_OK) return s;
-  return launch_pdl(gemm_fp4_kernel<BN, NV>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, 1, tmA, tmB, sfa, sfb, kb4,
-                    p);
+  s = launch_pdl(gemm_fp4_kernel<BN, NV>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, 1, tmA, tmB, sfa, sfb, kb4, p);
+  if (s != LPQ_OK || p.tail_s <= 1) return s;
+  return launch_tail_reduce<BN>(p, st);
 }
 
 }  // namespace
 
 // FP4 plan: 128 x 128 tiles on the natural operands (no swap; the scale
-// layouts of A and B are the same 128-row tiles); stream-K when a workspace is
-// given and the tiles do not divide evenly over the SMs.
+// layouts of A and B are the same 128-row tiles); whole tiles in waves, the
+// last partial wave split along K when a workspace is given.
 Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes) {
   Fp8Plan pl{};
   pl.transposed = 0;
@@ -258,19 +258,8 @@ Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes)
 
 lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, const uint8_t* sfa,
                       const uint8_t* sfb, int64_t K, GemmParams p, void* ws, cudaStream_t st) {
-  p.I = static_cast<int>(pl.I);
-  p.J = static_cast<int>(pl.J);
-  p.i_tiles = pl.i_tiles;
-  p.j_tiles = pl.j_tiles;
-  p.kblocks = pl.kblocks;
-  p.streamk = pl.streamk;
+  apply_plan(pl, p, ws);
   p.transposed = 0;
-  if (pl.streamk) {
-    const int tiles = pl.i_tiles * pl.j_tiles;
-    const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
-    p.counters = static_cast<int*>(ws);
-    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
-  }
   const int64_t kb4 = (K / (nv ? 16 : 32) + 3) / 4;
   if (nv) return launch_fp4_t<128, true>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
   return launch_fp4_t<128, false>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);

@@ -12,8 +12,9 @@
 //               accumulating a 128 x BN fp32 tile into one of two TMEM
 //               buffers, so the epilogue of tile t overlaps the K loop of t+1;
 //   warps 2-5   epilogue: tcgen05.ld -> scales -> bf16 -> global (or, for a
-//               stream-K piece, partial sums + an in-order combination by the
-//               last contributor of the tile).
+//               K slice, fp32 partial sums: to shared memory for a cluster
+//               split, summed over the cluster; to the workspace for a split
+//               tail tile, summed by the tail-reduction kernel).
 // Every barrier wait is bounded (a timeout sets the device error word and the
 // kernel winds down); no trap, no unbounded spin.
 #include <cuda_runtime.h>
@@ -219,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (!w.full && p.csplit <= 1) streamk_finish<BN>(p, w, quarter, lane);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -254,7 +254,9 @@ lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmP
   lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes,
                                   &done_mask);
   if (s != LPQ_OK) return s;
-  return launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, cluster, tmA, tmB, p);
+  s = launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, cluster, tmA, tmB, p);
+  if (s != LPQ_OK || p.tail_s <= 1) return s;
+  return launch_tail_reduce<BN>(p, st);
 }
 
 // Clusters of `S` CTAs of the BN kernel that can be resident at once
@@ -296,21 +298,26 @@ int max_active_clusters(int bn, int S) {
     case 16: return max_active_clusters_bn<16>(S);
     case 32: return max_active_clusters_bn<32>(S);
     case 64: return max_active_clusters_bn<64>(S);
+    case 128: return max_active_clusters_bn<128>(S);
+    case 256: return max_active_clusters_bn<256>(S);
     default: return 0;
   }
 }
 
 }  // namespace
 
-// Tile choice: swap-AB (weights on the tensor core's M side) for <= 256
-// tokens: N tile = the token count rounded up to 16 up to 64 tokens, 64 above
-// (several token tiles share each weight tile, visited back to back so the
-// weight rows are re-read from L2).  More tokens: 128 x 256 tiles.  Stream-K
-// (equal K-iteration ranges per CTA, partial tiles combined in a fixed order)
-// when a workspace is given and whole tiles would not divide evenly.
+// Tile choice: swap-AB (weights on the tensor core's M side) for <= 64
+// tokens, N tile = the token count rounded up to a power of two >= 16 (two
+// CTAs per SM).  More tokens: 128 x 256 tiles (from 65 to 256 tokens they
+// stage each weight tile into shared memory once or twice, where 128-token
+// swap-AB tiles would need 1/2 to 1/8 of the tensor rate per staged byte).
+// Few tiles (at most a quarter of the CTA slots): K split 4 or 8 ways across
+// a thread-block cluster whose CTAs add their partial sums through
+// distributed shared memory.  Otherwise whole tiles in waves, the last partial wave split along
+// K when a workspace is given (see finish_plan).
 Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes) {
   Fp8Plan pl{};
-  pl.transposed = (M <= 256);
+  pl.transposed = (M <= 64);
   pl.I = pl.transposed ? N : M;
   pl.J = pl.transposed ? M : N;
   int bn = 256;
@@ -321,37 +328,46 @@ Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, 
   pl.bn = bn;
   pl.ctas_per_sm = (bn <= 64) ? 2 : 1;     // Fp8Cfg<bn>::kCtasPerSm
   pl.kblocks = static_cast<int>((K + kBKBytes - 1) / kBKBytes);
-  if (pl.transposed) {
-    // decode: whole tiles when they fill at least half of the CTA slots;
-    // fewer tiles are split along K across a thread-block cluster whose
-    // CTAs add their partial sums through distributed shared memory
-    pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
-    pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
-    const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
-    const int slots = sm_count() * pl.ctas_per_sm;
-    pl.streamk = 0;
-    pl.csplit = 1;
-    pl.kb_per_split = pl.kblocks;
-    if (tiles * 2 <= slots && pl.kblocks >= 2) {
-      // the widest power-of-two split (8, 4 or 2: they pack evenly into the
-      // GPCs) that keeps tiles x split within the CTA slots and whose clusters
-      // fit on the GPU in at most two waves
-      for (int S = 8; S >= 2; S /= 2) {
-        if (tiles * S > slots || S > pl.kblocks) continue;
-        const int fit = max_active_clusters(pl.bn, S);
-        if (fit > 0 && tiles > 2 * fit) continue;   // (0: unknown / no device)
-        pl.kb_per_split = (pl.kblocks + S - 1) / S;
-        pl.csplit = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;   // no empty slice
-        break;
-      }
+  pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
+  pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
+  const int64_t tiles = static_cast<int64_t>(pl.i_tiles) * pl.j_tiles;
+  const int slots = sm_count() * pl.ctas_per_sm;
+  pl.csplit = 1;
+  pl.tail_s = 1;
+  pl.dp_tiles = static_cast<int>(tiles);
+  pl.kb_per_split = pl.kblocks;
+  if (tiles * 4 <= slots && pl.kblocks >= 4) {
+    // the widest power-of-two split (8 or 4: they pack evenly into the GPCs)
+    // that keeps tiles x split within the CTA slots and whose clusters fit
+    // on the GPU in at most two waves.  (A 2-way split measured slower than
+    // whole tiles: half a tile's partial sums per CTA cross the cluster.)
+    for (int S = 8; S >= 4; S /= 2) {
+      if (tiles * S > slots || S > pl.kblocks) continue;
+      const int fit = max_active_clusters(pl.bn, S);
+      if (fit > 0 && tiles > 2 * fit) continue;   // (0: unknown / no device)
+      pl.kb_per_split = (pl.kblocks + S - 1) / S;
+      pl.csplit = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;   // no empty slice
+      break;
     }
-    pl.grid = static_cast<int>(pl.csplit > 1 ? tiles * pl.csplit : std::min<int64_t>(tiles, slots));
+    if (pl.csplit > 1) {
+      pl.grid = static_cast<int>(tiles * pl.csplit);
+      return pl;
+    }
+    pl.kb_per_split = pl.kblocks;
+  }
+  if (pl.transposed) {
+    pl.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
     return pl;
   }
   finish_plan(pl, have_ws_budget, ws_bytes);
   return pl;
 }
 
+// Whole tiles in waves of one CTA per slot.  The tiles of the last, partial
+// wave leave CTAs idle; if at least twice as many CTAs as those tiles are
+// available (and a workspace is given), each of them is cut into S <= 8
+// equal K slices run by S CTAs, and a small reduction kernel adds the slices
+// in a fixed order.
 void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
   pl.i_tiles = static_cast<int>((pl.I + kBM - 1) / kBM);
   pl.j_tiles = static_cast<int>((pl.J + pl.bn - 1) / pl.bn);
@@ -359,45 +375,47 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes) {
   const int slots = sm_count() * (pl.ctas_per_sm > 0 ? pl.ctas_per_sm : 1);
   pl.csplit = 1;
   pl.kb_per_split = pl.kblocks;
-  pl.streamk = 0;
+  pl.tail_s = 1;
+  pl.dp_tiles = static_cast<int>(tiles);
   pl.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
-  if (have_ws && tiles % slots != 0) {
-    // full waves of whole tiles, then the leftover tiles' K iterations
-    // spread over every CTA
-    Fp8Plan sk = pl;
-    sk.streamk = 1;
-    const int64_t left_iters = (tiles % slots) * pl.kblocks;
-    sk.grid = static_cast<int>(tiles >= slots ? slots : std::min<int64_t>(left_iters, slots));
-    if (plan_ws_bytes(sk) <= ws_bytes) pl = sk;
-  }
+  const int64_t left = tiles % slots;
+  if (!have_ws || left == 0) return;
+  int S = static_cast<int>(std::min<int64_t>(8, slots / left));
+  S = std::min(S, pl.kblocks);
+  if (S < 2) return;
+  Fp8Plan t = pl;
+  t.kb_per_split = (pl.kblocks + S - 1) / S;
+  t.tail_s = (pl.kblocks + t.kb_per_split - 1) / t.kb_per_split;   // no empty slice
+  t.dp_tiles = static_cast<int>(tiles - left);
+  t.grid = static_cast<int>(tiles >= slots ? slots : left * t.tail_s);
+  if (plan_ws_bytes(t) <= ws_bytes) pl = t;
 }
 
 size_t plan_ws_bytes(const Fp8Plan& pl) {
-  if (!pl.streamk) return 0;
-  const size_t tiles = static_cast<size_t>(pl.i_tiles) * pl.j_tiles;
-  const size_t counters = (tiles * 4 * sizeof(int) + 255) / 256 * 256;
-  return counters + static_cast<size_t>(pl.grid) * 2 * 128 * pl.bn * sizeof(float);
+  if (pl.tail_s <= 1) return 0;
+  const size_t pieces = static_cast<size_t>(static_cast<int64_t>(pl.i_tiles) * pl.j_tiles - pl.dp_tiles) * pl.tail_s;
+  return pieces * 128 * pl.bn * sizeof(float);
 }
 
-lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
-                               void* ws, cudaStream_t st, bool b_static) {
+void apply_plan(const Fp8Plan& pl, GemmParams& p, void* ws) {
   p.I = static_cast<int>(pl.I);
   p.J = static_cast<int>(pl.J);
   p.i_tiles = pl.i_tiles;
   p.j_tiles = pl.j_tiles;
   p.kblocks = pl.kblocks;
-  p.streamk = pl.streamk;
-  p.transposed = pl.transposed;
-  p.j_fast = pl.transposed;
+  p.dp_tiles = pl.dp_tiles;
+  p.tail_s = pl.tail_s;
   p.csplit = pl.csplit;
   p.kb_per_split = pl.kb_per_split;
+  p.transposed = pl.transposed;
+  p.ws = pl.tail_s > 1 ? static_cast<float*>(ws) : nullptr;
+}
+
+lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
+                               void* ws, cudaStream_t st, bool b_static) {
+  apply_plan(pl, p, ws);
+  p.j_fast = pl.transposed;
   p.b_static = b_static ? 1 : 0;
-  if (pl.streamk) {
-    const int tiles = pl.i_tiles * pl.j_tiles;
-    const size_t counters = (static_cast<size_t>(tiles) * 4 * sizeof(int) + 255) / 256 * 256;
-    p.counters = static_cast<int*>(ws);
-    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
-  }
   switch (pl.bn) {
     case 16: return launch_bn<16>(tmA, tmB, p, pl.grid, st, pl.csplit);
     case 32: return launch_bn<32>(tmA, tmB, p, pl.grid, st, pl.csplit);

@@ -18,19 +18,22 @@ struct Fp8Plan {
   int bn;             // N tile of the tensor core
   int64_t I, J;       // rows of the A / B operands
   int i_tiles, j_tiles, kblocks;
-  int streamk;        // 1: equal K-iteration ranges per CTA (needs a workspace)
+  int dp_tiles;       // tiles dealt whole, in waves of `grid`
+  int tail_s;         // > 1: the other tiles split into this many K slices (needs a workspace)
   int ctas_per_sm;    // resident CTAs per SM the kernel is built for (grid = SMs x this)
   int csplit;         // > 1: K split across a cluster of this many CTAs (one tile per cluster)
-  int kb_per_split;   // K blocks per cluster rank
+  int kb_per_split;   // K blocks per slice (tail split or cluster rank)
   int grid;
 };
 
 Fp8Plan plan_fp8_rowscale(int64_t M, int64_t N, int64_t K, bool have_ws_budget, size_t ws_bytes);
-// workspace a plan needs (0 for data-parallel plans): tile counters + two
-// partial-sum slots per CTA
+// workspace a plan needs (0 without a tail split): one fp32 partial tile per
+// tail slice
 size_t plan_ws_bytes(const Fp8Plan& pl);
-// fill in tile counts / stream-K choice / grid for the given tiling
+// fill in tile counts / tail split / grid for the given tiling
 void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
+// copy a plan's decomposition into the kernel parameters
+void apply_plan(const Fp8Plan& pl, GemmParams& p, void* ws);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st, bool b_static = false);
 

@@ -1,5 +1,5 @@
 // gemm_noalloc.cu - lpq_gemm_scaled_noalloc: the FP8 row-scaled GEMM with
-// its stream-K scratch taken from a fixed array inside the library instead of
+// its split-K scratch taken from a fixed array inside the library instead of
 // a caller-provided workspace.
 //
 // Who needs this: a caller that cannot allocate device memory for a
@@ -8,15 +8,14 @@
 // the tensors of the operation, or a latency-critical path where cudaMalloc's
 // implicit device-wide synchronisation is not acceptable and no workspace was
 // reserved ahead of time.  Such a caller still passes its inputs and outputs;
-// only the stream-K partial sums and tile counters live here.
+// only the partial sums of split tail tiles live here.
 //
 // The scratch is a file-scope __device__ array of LPQ_NOALLOC_SCRATCH_BYTES
 // (16 MiB).  Every GPU that loads the library holds it until the process
-// exits.  All calls on a device share it and it keeps the previous call's
-// contents: the tile counters are cleared at the start of every call, and
-// calls that may run at the same time on the GPU (different streams without
-// ordering between them) race on it and give wrong results - order them on
-// one stream.
+// exits.  All calls on a device share it (no call reads what an earlier one
+// left), so calls that may run at the same time on the GPU (different
+// streams without ordering between them) race on it and give wrong results -
+// order them on one stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -92,12 +91,6 @@ lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream) {
   lpq_status s = scratch_ptr(&scratch);
   if (s != LPQ_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (pl.streamk) {
-    // tile counters must start at zero; a wound-down earlier call may have left them set
-    const size_t counters = (static_cast<size_t>(pl.i_tiles) * pl.j_tiles * 4 * sizeof(int) + 255) / 256 * 256;
-    cudaError_t e = cudaMemsetAsync(scratch, 0, counters, st);
-    if (e != cudaSuccess) return record_cuda(e);
-  }
 
   const void* opA = pl.transposed ? d->B : d->A;
   const void* opB = pl.transposed ? d->A : d->B;
@@ -115,7 +108,7 @@ lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream) {
   p.Y = d->Y;
   p.ldy = d->ldy;
   p.err = error_word_ptr();
-  return launch_fp8_rowscale(pl, tmA, tmB, p, pl.streamk ? scratch : nullptr, st);
+  return launch_fp8_rowscale(pl, tmA, tmB, p, pl.tail_s > 1 ? scratch : nullptr, st);
 }
 
 }  // extern "C"
