@@ -46,12 +46,15 @@ struct Fp4Cfg {
   static constexpr int kSfaBytes = kAtomsPerStage * kAtom;
   static constexpr int kSfbBytes = kBGroups * kAtomsPerStage * kAtom;
   static constexpr int kStageBytes = (kBM + BN) * kBKBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages = cmin(8, (200 * 1024) / kStageBytes);
-  // tensor-memory columns: 2 accumulators + per-stage scale slots (4 columns per atom)
+  static constexpr int kStages = cmin(8, (222 * 1024) / kStageBytes);
+  // tensor-memory columns: accumulators (two when they fit next to the scale
+  // slots, so the epilogue of one tile overlaps the next tile's K loop; one
+  // for 256-wide tiles) + per-stage scale slots (4 columns per atom)
   static constexpr int kSfaCols = kAtomsPerStage * 4;
   static constexpr int kSfbCols = kBGroups * kAtomsPerStage * 4;
   static constexpr int kSfCols = kStages * (kSfaCols + kSfbCols);
-  static constexpr int kNeedCols = 2 * BN + kSfCols;
+  static constexpr int kAccBufs = (2 * BN + kSfCols <= 512) ? 2 : 1;
+  static constexpr int kNeedCols = kAccBufs * BN + kSfCols;
   static constexpr int kTmemCols = kNeedCols <= 32 ? 32 : kNeedCols <= 64 ? 64 : kNeedCols <= 128 ? 128
                                    : kNeedCols <= 256 ? 256 : 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
@@ -61,6 +64,8 @@ struct Fp4Cfg {
                                      ((NV ? 0u : 1u) << 23) | (static_cast<uint32_t>(kBM >> 4) << 24);
 };
 static_assert(Fp4Cfg<128, true>::kNeedCols <= 512, "tensor memory budget");
+static_assert(Fp4Cfg<256, true>::kNeedCols <= 512 && Fp4Cfg<256, false>::kNeedCols <= 512, "tensor memory budget");
+static_assert(Fp4Cfg<256, true>::kSmemBytes <= 227 * 1024, "shared memory budget");
 
 template <int BN, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -133,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ksteps = min(4, ksteps_total - kb * 4);
           const int atoms = NV ? ksteps : (ksteps + 1) / 2;
           const uint32_t sf_bytes = atoms * kAtom;
-          mbar_arrive_expect_tx(full(stage), (kBM + BN) * kBKBytes + sf_bytes * (1 + C::kBGroups));
+          // 128-row groups of this B tile that exist in the scale buffer
+          const int bgroups = min(C::kBGroups, (p.J + 127) / 128 - w.j_tile * C::kBGroups);
+          mbar_arrive_expect_tx(full(stage), (kBM + BN) * kBKBytes + sf_bytes * (1 + bgroups));
           tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
           tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
           const int64_t atom0 = static_cast<int64_t>(kb) * C::kAtomsPerStage;
@@ -141,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    full(stage));
 #pragma unroll
           for (int g = 0; g < C::kBGroups; ++g)
-            bulk_g2s(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes),
+            if (g < bgroups)
+              bulk_g2s(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes),
                      sfb + ((w.j_tile * C::kBGroups + g) * sf_kb4 + atom0) * kAtom, sf_bytes, full(stage));
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      const uint32_t sf_base = tmem_base + 2 * BN;
+      const uint32_t sf_base = tmem_base + C::kAccBufs * BN;
       WorkIter wi(p, blockIdx.x, gridDim.x);
       Seg w;
       while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_cp_32x128b_warpx4(tsfa + a * 4, smem_desc(smem_u32(sSFA + stage * C::kSfaBytes + a * kAtom), 16, 128, 0));
 #pragma unroll
             for (int g = 0; g < C::kBGroups; ++g)
-              tc_cp_32x128b_warpx4(tsfb + (g * C::kAtomsPerStage + a) * 4,
+              tc_cp_32x128b_warpx4(tsfb + (a * C::kBGroups + g) * 4,
                                    smem_desc(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes + a * kAtom), 16,
                                              128, 0));
           }
@@ -188,11 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, 2);
             const uint32_t acc_in = (kb > w.kb0 || k > 0) ? 1u : 0u;
             if constexpr (NV) {
-              mma_nvf4(d, ad, bd, C::kIdesc, tsfa + k * 4, tsfb + k * 4, acc_in);
+              mma_nvf4(d, ad, bd, C::kIdesc, tsfa + k * 4, tsfb + k * 4 * C::kBGroups, acc_in);
             } else {
               const uint32_t id = static_cast<uint32_t>((k & 1) * 2);
               const uint32_t idesc = C::kIdesc | (id << 4) | (id << 29);
-              mma_mxf4(d, ad, bd, idesc, tsfa + (k >> 1) * 4, tsfb + (k >> 1) * 4, acc_in);
+              mma_mxf4(d, ad, bd, idesc, tsfa + (k >> 1) * 4, tsfb + (k >> 1) * 4 * C::kBGroups, acc_in);
             }
           }
           tc_commit(empty(stage));
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(tfull(acc));
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
       }
       tc_commit(drain);
       volatile int no_abort = 0;
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -242,13 +250,16 @@ lpq_status launch_fp4_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const ui
 
 }  // namespace
 
-// FP4 plan: 128 x 128 tiles on the natural operands (no swap; the scale
-// layouts of A and B are the same 128-row tiles); whole tiles in waves, the
-// last partial wave split along K when a workspace is given.
+// FP4 plan: 128 x 256 tiles on the natural operands (no swap; the scale
+// layouts of A and B are the same 128-row tiles).  A 256-wide tile doubles
+// the MMA work per scale copy of A and per staged byte of A over a 128-wide
+// one; the price is a single tensor-memory accumulator (the epilogue does not
+// overlap the next tile).  Whole tiles in waves, the last partial wave split
+// along K when a workspace is given.
 Fp8Plan plan_fp4(int64_t M, int64_t N, int64_t K, bool have_ws, size_t ws_bytes) {
   Fp8Plan pl{};
   pl.transposed = 0;
-  pl.bn = 128;
+  pl.bn = 256;
   pl.I = M;
   pl.J = N;
   pl.kblocks = static_cast<int>((K + kKPerStage - 1) / kKPerStage);
@@ -261,8 +272,8 @@ lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const 
   apply_plan(pl, p, ws);
   p.transposed = 0;
   const int64_t kb4 = (K / (nv ? 16 : 32) + 3) / 4;
-  if (nv) return launch_fp4_t<128, true>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
-  return launch_fp4_t<128, false>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
+  if (nv) return launch_fp4_t<256, true>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
+  return launch_fp4_t<256, false>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
 }
 
 }  // namespace lpq
