@@ -12,6 +12,10 @@
 // buffers hold per-group partial sums (NP of them, so the MMA of group kb+1..
 // overlaps the promotion of group kb) and the running accumulator lives in
 // the epilogue threads' registers (thread = output row, 128 of 256 columns).
+// The promotion is bound by the latency of tensor-memory loads (a load-and-
+// wait round trip costs ~140 cycles per warp); 128 x 128 tiles, which let a
+// warp issue all its loads of a group before one wait, measured slower
+// because they stage twice the operand bytes per MMA.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -171,10 +175,16 @@ __global__ void __maxnreg__(168)
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      // the group's two scales are loaded one group ahead, so their latency
+      // overlaps the previous group's promotion instead of preceding it
+      float sxv = row_ok ? __ldg(p.sx + m) : 0.0f;
+      float swv = nb_ok ? __ldg(p.sw + static_cast<int64_t>(nb) * p.kblocks) : 0.0f;
       for (int kb = 0; kb < p.kblocks; ++kb) {
-        const float sxv = row_ok ? __ldg(p.sx + static_cast<int64_t>(kb) * p.M + m) : 0.0f;
-        const float swv = nb_ok ? __ldg(p.sw + static_cast<int64_t>(nb) * p.kblocks + kb) : 0.0f;
         const float c = __fmul_rn(sxv, swv);
+        if (kb + 1 < p.kblocks) {
+          sxv = row_ok ? __ldg(p.sx + static_cast<int64_t>(kb + 1) * p.M + m) : 0.0f;
+          swv = nb_ok ? __ldg(p.sw + static_cast<int64_t>(nb) * p.kblocks + kb + 1) : 0.0f;
+        }
         if (!mbar_wait(pfull(pb), pphase, p.err, 0x304u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + pb * kBN + half * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
