@@ -199,6 +199,20 @@ typedef struct {
  * The GEMM may then start streaming B before that kernel has finished; its
  * activations, scales and output still wait for it.  FP8 row-scaled GEMMs. */
 #define LPQ_GEMM_B_STATIC 1u
+/* flags: A holds the bf16 activations X [M][lda] (lda in elements, a multiple
+ * of 16), not codes; the call quantizes them per token itself, by the rule of
+ * lpq_quantize_act_fp8 with LPQ_GRAN_ROW (s = max(max_k |x|, 1e-8) / 448,
+ * codes E4M3FN(x / s)), writes the scales to sa ([M] fp32, an output here) and
+ * computes the same Y as lpq_quantize_act_fp8 followed by lpq_gemm_scaled.
+ * fmt FP8, a_gran ROW, b_gran ROW only.  For M <= 16 the quantization runs
+ * inside the GEMM kernel and the codes never reach memory: the 8-bit
+ * activations do not make a round trip through HBM ("FP8 and INT8
+ * Inference", sections 6-9, where the quantization sits in the producing
+ * GEMM's epilogue; here it sits in the consuming GEMM, for bf16 activations
+ * from any producer).  For larger M the codes go through the workspace
+ * (lpq_gemm_workspace_bytes includes them; a missing or smaller workspace
+ * returns LPQ_ERR_WORKSPACE).  Not accepted by lpq_gemm_scaled_noalloc. */
+#define LPQ_GEMM_A_BF16 2u
 
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d);
 lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream);

@@ -30,9 +30,13 @@ struct GemmParams {
   int transposed;              // 0: Y[i][j], 1: Y[j][i]
   // epilogue scales: y = (acc * s_x) * s_w, s_x / s_w read from the i or j side
   const float* sx; int sx_stride;                // sx_stride 0: one scale for all
+  int sx_plain;                                  // sx points to shared memory (plain loads)
   const float* sw; int sw_stride;
   const float* gx; const float* gw;              // optional extra factors (NVFP4 g)
   uint16_t* Y; int64_t ldy;
+  // fused activation quantization (swap-AB, <= 16 tokens): bf16 activations
+  // [J][ldxa] quantized per token inside the kernel; scales written to sx_out
+  const uint16_t* xa; int64_t ldxa; float* sx_out;
   float* ws;                   // tail-split partials [tail tiles * tail_s][BN/4][128][4]
   uint32_t* err;
 };
@@ -117,13 +121,20 @@ __device__ __forceinline__ float scale_one(const GemmParams& p, float acc, float
   return a;
 }
 
+// Activation scale of token t (p.sx non-null): a global array, or the
+// kernel's own shared-memory copy when the quantization is fused.
+__device__ __forceinline__ float token_scale(const GemmParams& p, int64_t t) {
+  const int64_t k = t * p.sx_stride;
+  return p.sx_plain ? p.sx[k] : __ldg(p.sx + k);
+}
+
 template <int N>
 __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j0, const float (&v)[N]) {
   if (i >= p.I) return;
   const float g = p.gx ? __fmul_rn(__ldg(p.gx), __ldg(p.gw)) : 1.0f;
   if (!p.transposed) {
     // i = token row (x side), j = output channel (w side)
-    const float sxi = p.sx ? __ldg(p.sx + static_cast<int64_t>(i) * p.sx_stride) : 1.0f;
+    const float sxi = p.sx ? token_scale(p, i) : 1.0f;
     uint16_t* yrow = p.Y + static_cast<int64_t>(i) * p.ldy;
     if (j0 + N <= p.J) {
       uint32_t w[N / 2];
@@ -155,7 +166,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, int i, int j
 #pragma unroll
     for (int c = 0; c < N; ++c) {
       if (j0 + c < p.J) {
-        const float sxj = p.sx ? __ldg(p.sx + static_cast<int64_t>(j0 + c) * p.sx_stride) : 1.0f;
+        const float sxj = p.sx ? token_scale(p, j0 + c) : 1.0f;
         p.Y[static_cast<int64_t>(j0 + c) * p.ldy + i] =
             __bfloat16_as_ushort(__float2bfloat16_rn(scale_one(p, v[c], sxj, swi, g)));
       }

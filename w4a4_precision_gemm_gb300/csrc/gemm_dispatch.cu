@@ -33,7 +33,54 @@ lpq_status validate_common(const lpq_gemm_desc* d, int64_t kmult, int64_t ld_mul
   return LPQ_OK;
 }
 
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// LPQ_GEMM_A_BF16: A is bf16 and is quantized per token by the call itself:
+// inside the GEMM kernel for at most kFusedMaxTokens tokens, else into the
+// workspace by the standalone quantizer followed by the ordinary GEMM.
+lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st);
+
+lpq_status gemm_fp8_a_bf16(const lpq_gemm_desc* d, cudaStream_t st) {
+  lpq_status s = validate_common(d, 16, 16);
+  if (s != LPQ_OK) return s;
+  if (d->a_gran != LPQ_GRAN_ROW) return LPQ_ERR_UNSUPPORTED;
+  LPQ_CHECK_NULL(d->sa);
+  LPQ_CHECK_NULL(d->sb);
+  if ((reinterpret_cast<uintptr_t>(d->sa) & 3u) != 0) return LPQ_ERR_ALIGN;
+  const bool b_static = (d->flags & LPQ_GEMM_B_STATIC) != 0;
+  if (d->M <= kFusedMaxTokens) {
+    const Fp8Plan pl = plan_fp8_rowscale(d->M, d->N, d->K, false, 0);
+    CUtensorMap tmW;
+    if ((s = make_tmap_u8(&tmW, d->B, pl.I, d->K, d->ldb, 128, 128, true)) != LPQ_OK) return s;
+    GemmParams p{};
+    p.K = static_cast<int>(d->K);
+    p.sw = static_cast<const float*>(d->sb);
+    p.sw_stride = 1;
+    p.xa = static_cast<const uint16_t*>(d->A);
+    p.ldxa = d->lda;
+    p.sx_out = const_cast<float*>(static_cast<const float*>(d->sa));
+    p.Y = d->Y;
+    p.ldy = d->ldy;
+    p.err = error_word_ptr();
+    return launch_fp8_fused(pl, tmW, p, st, b_static);
+  }
+  const size_t codes = align256(static_cast<size_t>(d->M) * static_cast<size_t>(d->K));
+  if (!d->workspace || d->workspace_bytes < codes) return LPQ_ERR_WORKSPACE;
+  uint8_t* xq = static_cast<uint8_t*>(d->workspace);
+  s = lpq_quantize_act_fp8(static_cast<const uint16_t*>(d->A), d->M, d->K, d->lda, LPQ_GRAN_ROW, xq,
+                           const_cast<float*>(static_cast<const float*>(d->sa)), st);
+  if (s != LPQ_OK) return s;
+  lpq_gemm_desc q = *d;
+  q.A = xq;
+  q.lda = d->K;
+  q.flags = d->flags & ~LPQ_GEMM_A_BF16;
+  q.workspace = d->workspace_bytes > codes ? xq + codes : nullptr;
+  q.workspace_bytes = d->workspace_bytes - codes;
+  return gemm_fp8_rowscale(&q, st);
+}
+
 lpq_status gemm_fp8_rowscale(const lpq_gemm_desc* d, cudaStream_t st) {
+  if (d && (d->flags & LPQ_GEMM_A_BF16)) return gemm_fp8_a_bf16(d, st);
   lpq_status s = validate_common(d, 16, 16);
   if (s != LPQ_OK) return s;
   LPQ_CHECK_NULL(d->sa);
@@ -128,7 +175,10 @@ extern "C" {
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
   if (!d || d->M <= 0 || d->N <= 0 || d->K <= 0) return 0;
   if (is_fp8_rowscale(d)) {
-    return plan_ws_bytes(plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX));
+    const size_t plan = plan_ws_bytes(plan_fp8_rowscale(d->M, d->N, d->K, true, SIZE_MAX));
+    if ((d->flags & LPQ_GEMM_A_BF16) && d->M > kFusedMaxTokens)
+      return align256(static_cast<size_t>(d->M) * static_cast<size_t>(d->K)) + plan;
+    return (d->flags & LPQ_GEMM_A_BF16) ? 0 : plan;
   }
   if (is_fp4(d)) {
     return plan_ws_bytes(plan_fp4(d->M, d->N, d->K, true, SIZE_MAX));

@@ -51,10 +51,15 @@ static_assert(Fp8Cfg<64>::kCtasPerSm == 2 && Fp8Cfg<128>::kCtasPerSm == 1, "plan
 static_assert(2 * Fp8Cfg<64>::kSmemBytes <= 227 * 1024, "two CTAs must fit one SM's shared memory");
 static_assert(2 * Fp8Cfg<16>::kSmemBytes <= 227 * 1024, "two CTAs must fit one SM's shared memory");
 
-template <int BN>
+// FQ: fused activation quantization (swap-AB with BN = 16 only): operand B
+// is not loaded by TMA; the epilogue warps, idle during the K loop, compute
+// the tokens' scales and write every stage's E4M3 token tile into shared
+// memory themselves.
+template <int BN, bool FQ = false>
 __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
     gemm_fp8_rowscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const GemmParams p) {
+  static_assert(!FQ || BN == 16, "fused quantization: 16-token tiles, 8 threads per token");
   using C = Fp8Cfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -65,6 +70,10 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   // bars: full[S], empty[S], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // fused quantization: per-rank partial maxima [8][BN] (fp32 bits) and the
+  // tokens' scales [BN] (kFqExtraBytes of shared memory past the barriers)
+  uint32_t* fq_amax = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);   // [8][BN] per rank
+  float* fq_scale = reinterpret_cast<float*>(fq_amax + 8 * BN);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -76,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), FQ ? 5 : 1);      // FQ: + one arrival per token-writing warp
       mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -100,6 +109,11 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (FQ) {
+    // every CTA of the cluster is running before any writes into a peer's
+    // shared memory (the exchange of the tokens' partial maxima)
+    if (p.csplit > 1) cluster_sync();
+  }
   // Inputs of this call may come from the previous kernel on the stream:
   // every thread waits for it before touching global memory, except the TMA
   // thread when the weights are declared static, which first starts the
@@ -111,53 +125,65 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   }
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- producer
-      const uint64_t pol_a = p.transposed ? policy_evict_first() : policy_evict_last();
-      const uint64_t pol_b = p.transposed ? policy_evict_last() : policy_evict_first();
-      uint32_t stage = 0, phase = 0;
-      uint32_t issued = 0, issued_par = 0;   // per-stage: issued at least once / parity of last issue
-      bool ok = true;
-      WorkIter wi(p, blockIdx.x, gridDim.x);
-      Seg w;
-      // static weights: claim the first (still free) stages and start their
-      // weight tiles before waiting for the previous kernel; the token tiles of
-      // those stages follow after the wait
-      int pre = 0;
-      if (early_w) {
-        WorkIter wi2 = wi;
-        Seg w2;
-        bool h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
-        int kb2 = h2 ? w2.kb0 : 0;
-        while (h2 && pre < S) {
-          mbar_arrive_expect_tx(full(pre), C::kStageBytes);
-          if (p.transposed)
-            tma_load_2d(smem_u32(sA + pre * kBM * kBKBytes), &tmA, full(pre), kb2 * kBKBytes, w2.i_tile * kBM, pol_a);
-          else
-            tma_load_2d(smem_u32(sB + pre * BN * kBKBytes), &tmB, full(pre), kb2 * kBKBytes, w2.j_tile * BN, pol_b);
-          ++pre;
-          if (++kb2 == w2.kb1) {
-            h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
-            if (h2) kb2 = w2.kb0;
-          }
+    // ---------------------------------------------------------- producer
+    // (lane 0 issues; the other lanes only join the cluster barrier of a
+    // fused quantization)
+    constexpr uint32_t kTx = FQ ? kBM * kBKBytes : C::kStageBytes;   // FQ: B is written by the epilogue warps
+    const uint64_t pol_a = p.transposed ? policy_evict_first() : policy_evict_last();
+    const uint64_t pol_b = p.transposed ? policy_evict_last() : policy_evict_first();
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued = 0, issued_par = 0;   // per-stage: issued at least once / parity of last issue
+    bool ok = true;
+    WorkIter wi(p, blockIdx.x, gridDim.x);
+    Seg w;
+    // static weights: claim the first (still free) stages and start their
+    // weight tiles before waiting for the previous kernel; the token tiles of
+    // those stages follow after the wait
+    int pre = 0;
+    if (lane == 0 && early_w) {
+      WorkIter wi2 = wi;
+      Seg w2;
+      bool h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
+      int kb2 = h2 ? w2.kb0 : 0;
+      while (h2 && pre < S) {
+        mbar_arrive_expect_tx(full(pre), kTx);
+        if (p.transposed)
+          tma_load_2d(smem_u32(sA + pre * kBM * kBKBytes), &tmA, full(pre), kb2 * kBKBytes, w2.i_tile * kBM, pol_a);
+        else
+          tma_load_2d(smem_u32(sB + pre * BN * kBKBytes), &tmB, full(pre), kb2 * kBKBytes, w2.j_tile * BN, pol_b);
+        ++pre;
+        if (++kb2 == w2.kb1) {
+          h2 = wi2.next(p, blockIdx.x, gridDim.x, w2);
+          if (h2) kb2 = w2.kb0;
         }
-        pdl_wait();
-        pdl_launch();
       }
+      pdl_wait();
+      pdl_launch();
+    }
+    if constexpr (FQ) {
+      __syncwarp();
+      if (p.csplit > 1) cluster_sync();    // exchange of the tokens' partial maxima
+    }
+    if (lane == 0) {
       int n = 0;                              // stages handled so far
       while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++n) {
           if (n < pre) {
             // weight tile already on its way; add the token tile
-            if (p.transposed)
-              tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
-            else
-              tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+            if (!FQ) {
+              if (p.transposed)
+                tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN,
+                            pol_b);
+              else
+                tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM,
+                            pol_a);
+            }
           } else {
             if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x101u, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(full(stage), C::kStageBytes);
+            mbar_arrive_expect_tx(full(stage), kTx);
             tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
-            tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+            if (!FQ)
+              tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
           }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -172,6 +198,9 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
       }
     }
   } else if (warp == 1) {
+    if constexpr (FQ) {
+      if (p.csplit > 1) cluster_sync();    // exchange of the tokens' partial maxima
+    }
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -208,14 +237,101 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    const int et = threadIdx.x - 64;            // 0 .. 127
     uint32_t acc = 0, acc_phase = 0;
+    GemmParams pe = p;                          // FQ: scales from shared memory
+    uint32_t pstage = 0, pphase = 0;            // FQ: ring position of the token tiles
+    bool ok = true;
+    if constexpr (FQ) {
+      // ---- tokens' scales: s = max(max_k |x|, 1e-8) / 448, the per-token rule
+      // of the standalone quantizer.  8 threads per token; a cluster split
+      // takes each rank's K slice and exchanges the partial maxima.
+      const int ntok = p.J;
+      WorkIter wq(p, blockIdx.x, gridDim.x);
+      Seg w0;
+      const bool has = wq.next(p, blockIdx.x, gridDim.x, w0);
+      int k0 = 0, k1 = p.K;
+      if (p.csplit > 1 && has) {
+        k0 = w0.kb0 * kBKBytes;
+        k1 = min(p.K, w0.kb1 * kBKBytes);
+      }
+      // 8 threads per token (lanes 8g .. 8g+7 of a warp), 16-byte loads
+      const int tok = et >> 3, sub = et & 7;
+      float a = 0.0f;
+      if (tok < ntok) {
+        const uint16_t* xr = p.xa + static_cast<int64_t>(tok) * p.ldxa;
+#pragma unroll 4
+        for (int k = k0 + sub * 8; k < k1; k += 64) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr + k));
+          a = fmaxf(a, fmaxf(fmaxf(fmaxf(fabsf(bf16lo(u.x)), fabsf(bf16hi(u.x))), fmaxf(fabsf(bf16lo(u.y)), fabsf(bf16hi(u.y)))),
+                             fmaxf(fmaxf(fabsf(bf16lo(u.z)), fabsf(bf16hi(u.z))), fmaxf(fabsf(bf16lo(u.w)), fabsf(bf16hi(u.w))))));
+        }
+      }
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+      const uint32_t rank = p.csplit > 1 ? cluster_ctarank() : 0u;
+      if (sub == 0) {
+        if (p.csplit > 1) {
+          for (int r = 0; r < p.csplit; ++r)
+            st_dsmem_u32(map_to_rank(smem_u32(fq_amax + rank * BN + tok), static_cast<uint32_t>(r)), __float_as_uint(a));
+        } else {
+          fq_amax[tok] = __float_as_uint(a);
+        }
+      }
+      if (p.csplit > 1) {
+        __syncwarp();
+        cluster_sync();                         // every rank's maxima are in every rank
+      } else {
+        named_barrier_sync(1, 128);
+      }
+      if (et < BN) {
+        float m = 0.0f;
+        for (int r = 0; r < (p.csplit > 1 ? p.csplit : 1); ++r) m = fmaxf(m, __uint_as_float(fq_amax[r * BN + et]));
+        const float sc = __fdiv_rn(fmaxf(m, 1e-8f), 448.0f);
+        fq_scale[et] = sc;
+        if (p.sx_out && et < ntok && has && w0.i_tile == 0 && rank == 0) p.sx_out[et] = sc;
+      }
+      named_barrier_sync(1, 128);
+      pe.sx = fq_scale;
+      pe.sx_plain = 1;
+      pe.sx_stride = 1;
+    }
     WorkIter wi(p, blockIdx.x, gridDim.x);
     Seg w;
-    while (wi.next(p, blockIdx.x, gridDim.x, w)) {
-      if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x104u, abort_flag)) break;
+    while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
+      if constexpr (FQ) {
+        // ---- this piece's token tiles: 16 E4M3 codes per thread per stage,
+        // written in the 128-byte-swizzled K-major layout a TMA load gives
+        const int tok = et >> 3, c16 = et & 7;
+        const float sc = fq_scale[tok];
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!warp_wait(empty(pstage), pphase ^ 1u, p.err, 0x105u, abort_flag)) { ok = false; break; }
+          uint4 code = make_uint4(0u, 0u, 0u, 0u);
+          const int k = kb * kBKBytes + c16 * 16;
+          if (tok < p.J && k < p.K) {
+            const uint16_t* xp = p.xa + static_cast<int64_t>(tok) * p.ldxa + k;
+            const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(xp));
+            const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(xp + 8));
+            const uint32_t w32[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = cvt_e4m3x2(__fdiv_rn(bf16lo(w32[i]), sc), __fdiv_rn(bf16hi(w32[i]), sc));
+            code = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+          }
+          uint8_t* dst = sB + pstage * BN * kBKBytes + tok * kBKBytes + ((c16 ^ (tok & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = code;
+          fence_proxy_async_smem();             // visible to the tensor core's reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full(pstage));
+          if (++pstage == S) { pstage = 0; pphase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      if (!warp_wait(tfull(acc), acc_phase, p.err, 0x104u, abort_flag)) break;
       tc_fence_after();
       // a cluster split's partial goes to this CTA's (now idle) stage buffers
-      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane,
+      epilogue_tile<BN>(FQ ? pe : p, w, tmem_base + acc * BN, quarter, lane,
                         p.csplit > 1 ? reinterpret_cast<float*>(sA) : nullptr);
       tc_fence_before();
       __syncwarp();
@@ -233,8 +349,15 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
     if (warp >= 2) {
       WorkIter wi(p, blockIdx.x, gridDim.x);
       Seg w;
-      if (wi.next(p, blockIdx.x, gridDim.x, w))
-        cluster_reduce_store<BN>(p, w, smem_u32(sA), threadIdx.x - 64);
+      if (wi.next(p, blockIdx.x, gridDim.x, w)) {
+        GemmParams pr = p;
+        if (FQ) {
+          pr.sx = fq_scale;
+          pr.sx_plain = 1;
+          pr.sx_stride = 1;
+        }
+        cluster_reduce_store<BN>(pr, w, smem_u32(sA), threadIdx.x - 64);
+      }
     }
     __syncwarp();
     cluster_sync();                       // peers done reading this CTA's partial
@@ -246,15 +369,18 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int BN>
+constexpr int kFqExtraBytes = 1024;   // partial maxima and scales of a fused quantization
+static_assert(2 * (Fp8Cfg<16>::kSmemBytes + kFqExtraBytes) <= 227 * 1024, "two fused CTAs must fit one SM");
+
+template <int BN, bool FQ = false>
 lpq_status launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, cudaStream_t st,
                      int cluster) {
   using C = Fp8Cfg<BN>;
+  constexpr int kSmem = C::kSmemBytes + (FQ ? kFqExtraBytes : 0);
   static uint64_t done_mask = 0;
-  lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN>), C::kSmemBytes,
-                                  &done_mask);
+  lpq_status s = ensure_smem_attr(reinterpret_cast<const void*>(&gemm_fp8_rowscale_kernel<BN, FQ>), kSmem, &done_mask);
   if (s != LPQ_OK) return s;
-  s = launch_pdl(gemm_fp8_rowscale_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, cluster, tmA, tmB, p);
+  s = launch_pdl(gemm_fp8_rowscale_kernel<BN, FQ>, dim3(grid), dim3(kThreads), kSmem, st, cluster, tmA, tmB, p);
   if (s != LPQ_OK || p.tail_s <= 1) return s;
   return launch_tail_reduce<BN>(p, st);
 }
@@ -424,6 +550,14 @@ lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const 
     case 256: return launch_bn<256>(tmA, tmB, p, pl.grid, st, pl.csplit);
     default: return LPQ_ERR_UNSUPPORTED;
   }
+}
+
+lpq_status launch_fp8_fused(const Fp8Plan& pl, const CUtensorMap& tmW, GemmParams p, cudaStream_t st, bool b_static) {
+  if (!pl.transposed || pl.bn != 16 || pl.tail_s > 1) return LPQ_ERR_UNSUPPORTED;
+  apply_plan(pl, p, nullptr);
+  p.j_fast = 1;
+  p.b_static = b_static ? 1 : 0;
+  return launch_bn<16, true>(tmW, tmW, p, pl.grid, st, pl.csplit);
 }
 
 }  // namespace lpq

@@ -36,6 +36,12 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
 void apply_plan(const Fp8Plan& pl, GemmParams& p, void* ws);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st, bool b_static = false);
+// Most tokens the fused-quantization GEMM takes (one 16-token swap-AB tile).
+constexpr int64_t kFusedMaxTokens = 16;
+// FP8 row-scaled GEMM with the activations' per-token quantization inside the
+// kernel (p.xa / p.ldxa bf16, scales to p.sx_out); pl from plan_fp8_rowscale
+// for at most kFusedMaxTokens tokens, tmW over the weights.
+lpq_status launch_fp8_fused(const Fp8Plan& pl, const CUtensorMap& tmW, GemmParams p, cudaStream_t st, bool b_static);
 
 // Output tile width of the block-scaled FP8 kernel (two 128-column weight blocks).
 constexpr int kFp8BlockBN = 256;

@@ -67,7 +67,7 @@ lpq_status lpq_gemm_scaled_noalloc(const lpq_gemm_desc* d, void* stream) {
   LPQ_CHECK_NULL(d);
   const bool fp8_row = d->fmt == LPQ_FMT_FP8 &&
                        (d->a_gran == LPQ_GRAN_ROW || d->a_gran == LPQ_GRAN_TENSOR_STATIC) && d->b_gran == LPQ_GRAN_ROW;
-  if (!fp8_row) return LPQ_ERR_UNSUPPORTED;
+  if (!fp8_row || (d->flags & LPQ_GEMM_A_BF16)) return LPQ_ERR_UNSUPPORTED;   // codes only, no bf16 activations
   // the same argument rules as lpq_gemm_scaled for this format
   LPQ_CHECK_NULL(d->A);
   LPQ_CHECK_NULL(d->B);

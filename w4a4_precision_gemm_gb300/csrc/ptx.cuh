@@ -43,6 +43,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Barrier among `count` threads (whole warps) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Store to a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ void st_dsmem_u32(uint32_t caddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
 // Shared-memory address `saddr` of this CTA -> the same offset in CTA `rank`
 // of the cluster (a shared::cluster address).
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
@@ -116,6 +124,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
       }
     }
   }
+}
+
+// Warp-wide form of mbar_wait: lane 0 polls the barrier and every lane gets
+// the outcome (32 threads polling one barrier slow the copy and MMA
+// completions that land on the same barriers).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t where,
+                                          volatile int* abort_flag) {
+  int r = 0;
+  if ((threadIdx.x & 31) == 0) r = mbar_wait(bar, parity, err, where, abort_flag) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, r, 0) != 0;
 }
 
 // ------------------------------------------------------------------ TMA ----

@@ -23,6 +23,7 @@ LPQ_OK, LPQ_ERR_NULL, LPQ_ERR_SHAPE, LPQ_ERR_ALIGN, LPQ_ERR_UNSUPPORTED, LPQ_ERR
 GRAN_ROW, GRAN_BLOCK_1x128, GRAN_BLOCK_128x128, GRAN_TENSOR_STATIC = range(4)
 FMT_FP8, FMT_INT8, FMT_NVFP4, FMT_MXFP4 = range(4)
 GEMM_B_STATIC = 1
+GEMM_A_BF16 = 2
 
 EXPORTS = (
     "lpq_status_string", "lpq_last_cuda_error", "lpq_read_error_word", "lpq_clear_error_word",
@@ -315,9 +316,10 @@ def gemm_scaled(fmt, a_gran, b_gran, A, B, sa, sb, *, M, N, K, ga=None, gb=None,
     return Y
 
 
-def workspace_for(fmt, a_gran, b_gran, M, N, K, device="cuda"):
+def workspace_for(fmt, a_gran, b_gran, M, N, K, device="cuda", flags=0):
     """A zero-filled workspace tensor of the size lpq_gemm_workspace_bytes reports."""
     d = GemmDesc()
     d.fmt, d.a_gran, d.b_gran, d.M, d.N, d.K = int(fmt), int(a_gran), int(b_gran), int(M), int(N), int(K)
+    d.flags = int(flags)
     n = lpq_gemm_workspace_bytes(d)
     return torch.zeros((max(n, 16),), dtype=torch.uint8, device=device)
