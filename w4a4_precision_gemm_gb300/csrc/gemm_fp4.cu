@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     WorkIter wi(p, blockIdx.x, gridDim.x);
     Seg w;
     while (wi.next(p, blockIdx.x, gridDim.x, w)) {
-      if (!mbar_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
+      if (!warp_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
       tc_fence_after();
       epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
       tc_fence_before();

@@ -185,7 +185,7 @@ __global__ void __maxnreg__(168)
           sxv = row_ok ? __ldg(p.sx + static_cast<int64_t>(kb + 1) * p.M + m) : 0.0f;
           swv = nb_ok ? __ldg(p.sw + static_cast<int64_t>(nb) * p.kblocks + kb + 1) : 0.0f;
         }
-        if (!mbar_wait(pfull(pb), pphase, p.err, 0x304u, abort_flag)) { ok = false; break; }
+        if (!warp_wait(pfull(pb), pphase, p.err, 0x304u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + pb * kBN + half * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll
