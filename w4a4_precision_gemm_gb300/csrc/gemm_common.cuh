@@ -227,8 +227,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Seg& w,
 // 32 lanes of a warp read 512 contiguous bytes of each slice.
 template <int BN>
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const GemmParams p) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   constexpr int kQ = 128 * (BN / 4);            // float4 groups per tile
   const int tail_tiles = p.i_tiles * p.j_tiles - p.dp_tiles;
   const int64_t total = static_cast<int64_t>(tail_tiles) * kQ;

@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();      // inputs of this call may come from the previous kernel
   pdl_launch();
+  pdl_wait();      // inputs of this call may come from the previous kernel
   // MMA k-steps (64 elements) in the last, possibly partial, stage
   const int ksteps_total = (p.K + 63) / 64;
 

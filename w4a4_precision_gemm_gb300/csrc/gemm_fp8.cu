@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
   // weight stream of its opening stages (see the producer below).
   const bool early_w = p.b_static && warp == 0 && lane == 0;
   if (!early_w) {
-    pdl_wait();
     pdl_launch();
+    pdl_wait();
   }
 
   if (warp == 0) {
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(kThreads, Fp8Cfg<BN>::kCtasPerSm)
           if (h2) kb2 = w2.kb0;
         }
       }
-      pdl_wait();
       pdl_launch();
+      pdl_wait();
     }
     if constexpr (FQ) {
       __syncwarp();

@@ -98,8 +98,8 @@ __global__ void __maxnreg__(168)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();      // inputs of this call may come from the previous kernel
   pdl_launch();
+  pdl_wait();      // inputs of this call may come from the previous kernel
   const int tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {

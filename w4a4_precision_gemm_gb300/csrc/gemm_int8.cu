@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   __syncthreads();
-  pdl_wait();      // inputs of this call may come from the previous kernel
   pdl_launch();
+  pdl_wait();      // inputs of this call may come from the previous kernel
   const int tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {

@@ -29,7 +29,11 @@ __device__ __forceinline__ uint32_t lane_id() {
 // serialization: it may start while the previous kernel on the stream is
 // still running.  pdl_wait() blocks until that kernel has finished and its
 // memory is visible, so each thread calls it before its first access to
-// global memory; pdl_launch() then lets the next kernel begin launching.
+// global memory.  Each kernel calls pdl_launch() first, so that the next
+// kernel on the stream can become resident, set up and start its static
+// weight stream while this one still runs: its own pdl_wait() then waits for
+// this kernel's end, which comes after this kernel's wait for its
+// predecessor, so every read still sees every earlier kernel's writes.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -153,8 +153,8 @@ template <int MODE>
 __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t* __restrict__ X, int K, int64_t ldx,
                                                           const float* __restrict__ smooth, uint8_t* __restrict__ Q,
                                                           float* __restrict__ S) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   __shared__ float red[32];
   const int64_t row = blockIdx.x;
   const uint16_t* xr = X + row * ldx;
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t* __restr
 __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t* __restrict__ X, int64_t M,
                                                                  int64_t K, int64_t ldx, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t kg = blockIdx.y;
   const int sub = lane & 15;
@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t*
 __global__ void __launch_bounds__(256) quant_fp8_block128_kernel(const uint16_t* __restrict__ W, int64_t N,
                                                                  int64_t K, int64_t ldw, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   __shared__ float red[8];
   const int64_t nb = blockIdx.y, kb = blockIdx.x;
   const int col8 = threadIdx.x & 15;
@@ -298,8 +298,8 @@ __device__ __forceinline__ int seg_chunk(int j) {
 __global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* __restrict__ X, int64_t K,
                                                                int64_t ldx, const float* __restrict__ S,
                                                                uint8_t* __restrict__ Q) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const int cpr = static_cast<int>(K / 8);
   const float s = __ldg(S);
@@ -328,8 +328,8 @@ __global__ void __launch_bounds__(256) quant_fp8_static_kernel(const uint16_t* _
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
                                                           int64_t ldx, float* __restrict__ out) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   __shared__ float red[32];
   const int cpr = static_cast<int>(K / 8);
   float a = 0.0f;
@@ -360,8 +360,8 @@ __device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t kb4) {
 __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __restrict__ X, int64_t K, int64_t ldx,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
                                                           float* __restrict__ gs) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const int cpr = static_cast<int>(K / 8);
   const float amax = gs[0];
@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __rest
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t K, int64_t ldx,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const int cpr = static_cast<int>(K / 8);
   Chunk8 c[kCPT];
@@ -460,8 +460,8 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __rest
 // Zero the padding of a scale-factor buffer: rows [rows, rows_pad) of every
 // tile and blocks [kblocks, kb4*4) of every row.
 __global__ void sf_pad_kernel(uint8_t* __restrict__ SF, int64_t rows, int64_t kblocks) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t kb4 = (kblocks + 3) / 4;
   const int64_t rows_pad = (rows + 127) / 128 * 128;
   const int64_t n = rows_pad * kb4 * 4;

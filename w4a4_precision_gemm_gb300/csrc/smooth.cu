@@ -20,8 +20,8 @@ namespace {
 __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restrict__ X, int64_t rows, int64_t K,
                                                          int64_t ld, int64_t rows_per_slice,
                                                          unsigned int* __restrict__ out) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c8 * 8 >= K) return;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_slice;
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restr
 
 // s_j from ax_j and aw_j (aw held in s on entry), fp64 power, one rounding.
 __global__ void smooth_finalize_kernel(const float* __restrict__ ax, float* __restrict__ s, int64_t K, float alpha) {
-  pdl_wait();
   pdl_launch();
+  pdl_wait();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= K) return;
   const double a = static_cast<double>(alpha);
