@@ -206,41 +206,42 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t* __restr
 }
 
 // ------------------------------------------------------------------------
-// FP8 per 1x128 group.  Grid (ceil(M/64), K/128): a CTA covers 64 rows of one
-// K group; a warp covers 8 rows, two per pass (half-warp = one 128-element
-// group, 8 elements per lane).  The scale is stored K-group major,
-// S[kg * M + row], so consecutive rows give consecutive scale stores.
+// FP8 per 1x128 group, on the row-segment mapping (declared below with the
+// other segment kernels): for each j the 16 lanes 16g..16g+15 of a warp hold
+// the 16 chunks of one 128-element group, so a half-warp reduces a group and
+// every CTA reads a contiguous stretch of one row.  The scale is stored
+// K-group major, S[kg * M + row] (the layout the block-scaled GEMM reads).
 // ------------------------------------------------------------------------
+__device__ __forceinline__ int seg_chunk(int j);
+
 __global__ void __launch_bounds__(256) quant_fp8_group128_kernel(const uint16_t* __restrict__ X, int64_t M,
                                                                  int64_t K, int64_t ldx, uint8_t* __restrict__ Q,
                                                                  float* __restrict__ S) {
   pdl_launch();
   pdl_wait();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t kg = blockIdx.y;
-  const int sub = lane & 15;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 64 + warp * 8 + (lane >> 4);
-  const int64_t col = kg * 128 + sub * 8;
+  const int64_t row = blockIdx.x;
+  const int cpr = static_cast<int>(K / 8);
+  const int lane = threadIdx.x & 31;
   Chunk8 c[kCPT];
 #pragma unroll
   for (int j = 0; j < kCPT; ++j) {
-    const int64_t row = r0 + 2 * j;
-    if (row < M) c[j] = load_bf16x8_stream(X + row * ldx + col);
+    const int c8 = seg_chunk(j);
+    if (c8 < cpr) c[j] = load_bf16x8_stream(X + row * ldx + static_cast<int64_t>(c8) * 8);
     else zero8(c[j]);
   }
 #pragma unroll
   for (int j = 0; j < kCPT; ++j) {
-    const int64_t row = r0 + 2 * j;
+    const int c8 = seg_chunk(j);
     float a = amax8(c[j]);
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     const float s = __fdiv_rn(fmaxf(a, kScaleFloor), 448.0f);
-    if (row < M) {
-      if (sub == 0) S[kg * M + row] = s;
+    if (c8 < cpr) {
+      if ((lane & 15) == 0) S[static_cast<int64_t>(c8 >> 4) * M + row] = s;
       float q[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(c[j].v[i], s);
-      *reinterpret_cast<uint2*>(Q + row * K + col) = e4m3x8(q);
+      *reinterpret_cast<uint2*>(Q + row * K + static_cast<int64_t>(c8) * 8) = e4m3x8(q);
     }
   }
 }
@@ -569,9 +570,11 @@ lpq_status lpq_quantize_act_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t
     case LPQ_GRAN_ROW:
       return launch_row(0, X, M, K, ldx, nullptr, Xq, sx, st);
     case LPQ_GRAN_BLOCK_1x128: {
-      if (K / 128 > 65535) return LPQ_ERR_SHAPE;
-      const dim3 grid(static_cast<unsigned>((M + 63) / 64), static_cast<unsigned>(K / 128));
-      return launch_pdl(quant_fp8_group128_kernel, grid, dim3(256), 0, st, 1, X, M, K, ldx, Xq, sx);
+      const SegShape sh = seg_shape(K);
+      if (sh.segs > 65535u) return LPQ_ERR_SHAPE;
+      const dim3 grid(static_cast<unsigned>(M), sh.segs);
+      return launch_pdl(quant_fp8_group128_kernel, grid, dim3(static_cast<unsigned>(sh.threads)), 0, st, 1, X, M, K,
+                        ldx, Xq, sx);
     }
     case LPQ_GRAN_TENSOR_STATIC: {
       const SegShape sh = seg_shape(K);
