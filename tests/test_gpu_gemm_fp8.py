@@ -164,3 +164,23 @@ def test_fp8_static_weights_flag(M, N, K):
     yr, b = _ref(qxo, sxo, qwo, swo)
     ok, worst = G.check(bf16_to_f64(host(outs[1])), yr, b)
     assert ok.all(), worst
+
+
+def test_fp8_activations_larger_than_l2():
+    """69 MB of activation codes and 4 MB of weights: weight-column-fastest
+    tile order.  A sample of rows against the oracle."""
+    L = lpq()
+    M, N, K = 8448, 512, 8192
+    xb = synth.activations(M, K, 7200, n_outlier=8, lo=50, hi=500)
+    wb = synth.weights(N, K, 7201)
+    qx, sx = Q.fp8_per_row(synth.f32_from_bf16_bits(xb))
+    qw, sw = Q.fp8_per_row(synth.f32_from_bf16_bits(wb))
+    ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
+    Y = L.gemm_scaled(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, dev(qx), dev(qw), dev(sx), dev(sw), M=M, N=N, K=K,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    assert L.lpq_read_error_word() == 0
+    rows = np.arange(0, M, 97)
+    yr, b = _ref(qx[rows], sx[rows], qw, sw)
+    ok, worst = G.check(bf16_to_f64(host(Y)[rows]), yr, b)
+    assert ok.all(), worst

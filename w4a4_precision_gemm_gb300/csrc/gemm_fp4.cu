@@ -271,6 +271,7 @@ lpq_status launch_fp4(bool nv, const Fp8Plan& pl, const CUtensorMap& tmA, const 
                       const uint8_t* sfb, int64_t K, GemmParams p, void* ws, cudaStream_t st) {
   apply_plan(pl, p, ws);
   p.transposed = 0;
+  p.j_fast = j_fastest(pl.I, pl.J, K, 0.5) ? 1 : 0;
   const int64_t kb4 = (K / (nv ? 16 : 32) + 3) / 4;
   if (nv) return launch_fp4_t<256, true>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);
   return launch_fp4_t<256, false>(tmA, tmB, sfa, sfb, kb4, p, pl.grid, st);

@@ -540,7 +540,7 @@ void apply_plan(const Fp8Plan& pl, GemmParams& p, void* ws) {
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st, bool b_static) {
   apply_plan(pl, p, ws);
-  p.j_fast = pl.transposed;
+  p.j_fast = pl.transposed ? 1 : (j_fastest(pl.I, pl.J, p.K, 1.0) ? 1 : 0);
   p.b_static = b_static ? 1 : 0;
   switch (pl.bn) {
     case 16: return launch_bn<16>(tmA, tmB, p, pl.grid, st, pl.csplit);

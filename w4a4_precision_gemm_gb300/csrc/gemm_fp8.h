@@ -36,6 +36,17 @@ void finish_plan(Fp8Plan& pl, bool have_ws, size_t ws_bytes);
 void apply_plan(const Fp8Plan& pl, GemmParams& p, void* ws);
 lpq_status launch_fp8_rowscale(const Fp8Plan& pl, const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p,
                                void* ws, cudaStream_t st, bool b_static = false);
+// Tile visiting order for an [I x K] by [J x K] product (bytes per element of
+// the operands given): consecutive tiles share the A rows (J fastest) when A
+// is too large to stay in L2 while the B operand fits, so that every A row
+// block is read from DRAM once and B is re-read from L2; otherwise they share
+// the B rows (I fastest).
+inline bool j_fastest(int64_t I, int64_t J, int64_t K, double bytes_per_elem) {
+  const double a = static_cast<double>(I) * K * bytes_per_elem, b = static_cast<double>(J) * K * bytes_per_elem;
+  constexpr double kL2Share = 64.0 * 1024 * 1024;   // half the L2
+  return a > kL2Share && b <= kL2Share;
+}
+
 // Most tokens the fused-quantization GEMM takes (one 16-token swap-AB tile).
 constexpr int64_t kFusedMaxTokens = 16;
 // FP8 row-scaled GEMM with the activations' per-token quantization inside the

@@ -43,6 +43,7 @@ constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) 
 struct BlockParams {
   int M, N, K;
   int m_tiles, n_tiles, kblocks;
+  int n_fast;         // tile order: 1 = consecutive tiles share the activation rows
   const float* sx;    // [K/128][M]
   const float* sw;    // [ceil(N/128)][K/128]
   uint16_t* Y;
@@ -109,7 +110,7 @@ __global__ void __maxnreg__(168)
       uint32_t stage = 0, phase = 0, issued = 0, issued_par = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+        const int mt = p.n_fast ? t / p.n_tiles : t % p.m_tiles, nt = p.n_fast ? t % p.n_tiles : t / p.m_tiles;
         for (int kb = 0; kb < p.kblocks; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, 0x301u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(full(stage), kStageBytes);
@@ -167,7 +168,7 @@ __global__ void __maxnreg__(168)
     ep.Y = p.Y;
     ep.ldy = p.ldy;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+      const int mt = p.n_fast ? t / p.n_tiles : t % p.m_tiles, nt = p.n_fast ? t % p.n_tiles : t / p.m_tiles;
       const int m = mt * kBM + row_in_tile;
       const bool row_ok = m < p.M;
       const int nb = nt * 2 + half;
@@ -240,6 +241,7 @@ lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int6
   p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.kblocks = static_cast<int>(K / kBK);
+  p.n_fast = j_fastest(M, N, K, 1.0) ? 1 : 0;
   p.sx = sx;
   p.sw = sw;
   p.Y = Y;
