@@ -246,7 +246,7 @@ class Workload:
 
 
 def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
-    """FP8 W8A8 decode: per-token act quant + swap-AB / stream-K FP8 GEMM."""
+    """FP8 W8A8 decode: per-token act quant + the FP8 GEMM (swap-AB up to 64 tokens, cluster K split for few tiles)."""
     W = Workload(wl.name, L, torch)
     W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
                 "act": "fp8 e4m3 per-token dynamic", "weight": "fp8 e4m3 per-channel static",

@@ -46,7 +46,7 @@ SHAPES = [
     (16, 256, 256),        # the tiny W8A8 configuration
     (1, 128, 128), (1, 4096, 4096), (5, 200, 336), (16, 6144, 4096), (64, 4096, 14336),
     (200, 1000, 1024), (256, 4096, 4096), (300, 520, 4096), (1000, 4096, 2048), (517, 384, 144),
-    (130, 12288, 512), (256, 19968, 1024),   # swap-AB with 256-token tiles: stream-K tail / one wave + 4 tiles
+    (130, 12288, 512), (256, 19968, 1024),   # 96 tiles (one partial wave) / one wave + 4 tiles: K-split tail
     (1152, 4352, 256),                       # 153 tiles: one wave, then fewer leftover K iterations than CTAs
 ]
 
