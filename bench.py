@@ -245,12 +245,35 @@ class Workload:
         return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).cuda()
 
 
+def workload_config(name: str) -> dict:
+    """The `config` object of a workload's JSON line (no device needed: the
+    reference arm prints the same one)."""
+    if name == "decode_fp8":
+        wl = CFG.DECODE_FP8
+        return {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "act": "fp8 e4m3 per-token dynamic", "weight": "fp8 e4m3 per-channel static",
+                "l2": "inputs larger than L2: 872 MB of distinct FP8 weights streamed per step"}
+    if name in ("nvfp4", "mxfp4"):
+        wl = CFG.NVFP4_W4A4 if name == "nvfp4" else CFG.MXFP4_W4A4
+        return {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "format": wl.fmt, "l2": "inputs larger than L2 for M=8192; M=512 weights 37-117 MB"}
+    if name == "prefill_fp8_block":
+        wl = CFG.PREFILL_FP8_BLOCK
+        return {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "act": "fp8 e4m3 per 1x128 group, dynamic", "weight": "fp8 e4m3 per 128x128 block",
+                "l2": "inputs larger than L2 (M=8192 activations 64-235 MB bf16; weights 17-117 MB fp8)"}
+    if name == "int8_smoothquant":
+        wl = CFG.INT8_SMOOTHQUANT
+        return {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
+                "alpha": CFG.SMOOTH_ALPHA, "calibration_tokens": CFG.INT8_CALIB_TOKENS,
+                "l2": "inputs larger than L2 for M=4096 (W 16-117 MB int8, X 32 MB bf16)"}
+    raise KeyError(name)
+
+
 def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
     """FP8 W8A8 decode: per-token act quant + the FP8 GEMM (swap-AB up to 64 tokens, cluster K split for few tiles)."""
     W = Workload(wl.name, L, torch)
-    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
-                "act": "fp8 e4m3 per-token dynamic", "weight": "fp8 e4m3 per-channel static",
-                "l2": "inputs larger than L2: 872 MB of distinct FP8 weights streamed per step"}
+    W.config = workload_config("decode_fp8")
     W.dominant = "gemm_fp8"
     W.dominant_bound = "hbm"
     W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
@@ -284,8 +307,7 @@ def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
 def build_fp4(L, torch, wl):
     nv = wl.fmt == "nvfp4"
     W = Workload(wl.name, L, torch)
-    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
-                "format": wl.fmt, "l2": "inputs larger than L2 for M=8192; M=512 weights 37-117 MB"}
+    W.config = workload_config(wl.fmt)
     W.dominant = "gemm_fp4"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "fp4"
@@ -328,9 +350,7 @@ def build_fp4(L, torch, wl):
 def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
     """FP8 prefill with 1x128 activation / 128x128 weight block scales."""
     W = Workload(wl.name, L, torch)
-    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
-                "act": "fp8 e4m3 per 1x128 group, dynamic", "weight": "fp8 e4m3 per 128x128 block",
-                "l2": "inputs larger than L2 (M=8192 activations 64-235 MB bf16; weights 17-117 MB fp8)"}
+    W.config = workload_config("prefill_fp8_block")
     W.dominant = "gemm_fp8_block"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "fp8"
@@ -367,9 +387,7 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
     quantization at load; per step the smoothed per-token quantizer and the
     INT8 GEMM."""
     W = Workload(wl.name, L, torch)
-    W.config = {"workload": wl.name, "Ms": list(wl.Ms), "KNs": [list(x) for x in wl.KNs],
-                "alpha": CFG.SMOOTH_ALPHA, "calibration_tokens": CFG.INT8_CALIB_TOKENS,
-                "l2": "inputs larger than L2 for M=4096 (W 16-117 MB int8, X 32 MB bf16)"}
+    W.config = workload_config("int8_smoothquant")
     W.dominant = "gemm_int8"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "int8"
@@ -493,7 +511,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
+            "data": "synthetic",
+            "config": dict(workload_config(args.workload), parallelism=f"replicas x{max(1, args.gpus)}"),
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
