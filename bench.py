@@ -127,7 +127,7 @@ TRAFFIC_FILES = {"gemm_fp8": "gemm_fp8_decode_traffic.txt", "gemm_fp4": "gemm_fp
 KERNEL_SOURCES = {"gemm_fp8": ["gemm_fp8.cu", "gemm_common.cuh", "ptx.cuh"],
                   "gemm_fp4": ["gemm_fp4.cu", "gemm_common.cuh", "ptx.cuh"],
                   "gemm_fp8_block": ["gemm_fp8_block.cu", "gemm_common.cuh", "ptx.cuh"],
-                  "gemm_int8": ["gemm_int8.cu", "gemm_common.cuh", "ptx.cuh"]}
+                  "gemm_int8": ["gemm_int8_tc.cu", "gemm_common.cuh", "ptx.cuh"]}
 
 
 def kernel_source_hash(kind: str) -> str:
@@ -382,10 +382,16 @@ def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
     return W
 
 
+def _int8_probe_desc(L, M, N, K, flags):
+    d = L.GemmDesc()
+    d.fmt, d.a_gran, d.b_gran, d.M, d.N, d.K, d.flags = L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, M, N, K, flags
+    return d
+
+
 def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
-    """INT8 W8A8 with SmoothQuant: calibration and smoothed weight
-    quantization at load; per step the smoothed per-token quantizer and the
-    INT8 GEMM."""
+    """INT8 W8A8 with SmoothQuant: calibration, smoothed weight quantization
+    and the weights' digit planes at load; per step the smoothed per-token
+    quantizer and the INT8 GEMM (tensor cores, exact int32 result)."""
     W = Workload(wl.name, L, torch)
     W.config = workload_config("int8_smoothquant")
     W.dominant = "gemm_int8"
@@ -400,8 +406,14 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
         Wd = W.dev_bf16(CFG.make_w(wl, N, K, salt=si))
         sm = L.smooth_calibrate(amax, Wd, CFG.SMOOTH_ALPHA)
         Wq, sw = L.quantize_weight_int8(Wd, sm)
-        wq[si] = (Wq, sw, sm)
-        del Wd
+        planes = L.int8_weight_planes(Wq)        # the tensor-core GEMM's digit planes, at load time too
+        wq[si] = (planes, sw, sm)
+        del Wd, Wq
+    flags = L.GEMM_B_INT8_PLANES
+    ws_bytes = max(L.lpq_gemm_workspace_bytes(_int8_probe_desc(L, M, N, K, flags))
+                   for M in wl.Ms for (K, N) in wl.KNs)
+    ws = torch.zeros((ws_bytes,), dtype=torch.uint8, device="cuda")   # shared: the calls run in order
+    W.keep = [ws]
     for mi, M in enumerate(wl.Ms):
         for si, (K, N) in enumerate(wl.KNs):
             Wq, sw, sm = wq[si]
@@ -410,7 +422,8 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
             Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
             sx = torch.empty((M,), dtype=torch.float32, device="cuda")
             Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-            desc = L.make_desc(L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
+            desc = L.make_desc(L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws,
+                               flags=flags)
             W.keep = getattr(W, "keep", []) + [desc, Wq, sw, sm, Xq, sx, Y]
             W.calls.append(dict(kind="quant_int8_smooth", M=M, K=K, N=N,
                                 fn=(lambda Xd=Xd, Xq=Xq, sx=sx, sm=sm: L.lpq_quantize_act_int8(Xd, sm, Xq, sx)),
@@ -688,13 +701,19 @@ def main():
         ratio = NOMINAL_RATIO[getattr(W, "dominant_dtype", "fp8")]
         peak, unit = peaks["bf16_tflops"] * ratio, "TFLOP/s"
     peak_src = f"{peaks['src']} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops x nominal ratio'})"
+    extra = {}
     if getattr(W, "dominant_dtype", "") == "int8":
-        # no tcgen05 INT8 on this part: the INT8 tensor rate is measured here,
-        # as the vendor library's INT8 GEMM (cuBLASLt via torch._int_mm, 8192^3)
-        peak, peak_src = measure_int8_library_peak(torch), "measured live: torch._int_mm 8192^3 (cuBLASLt INT8)"
+        # no tcgen05 INT8 MMA on this part: the GEMM runs four E4M3 MMAs per
+        # int8 product (digit planes), so its tensor roofline in int8
+        # operations is the FP8 rate / 4; the vendor library's INT8 GEMM
+        # (legacy int8 MMA) is measured live for context
+        peak = peaks["bf16_tflops"] * NOMINAL_RATIO["fp8"] / 4
+        peak_src = f"{peaks['src']} (bf16_tflops x 2 for FP8, / 4 E4M3 MMAs per int8 product)"
+        extra["library_int8_tops"] = measure_int8_library_peak(torch)
+        extra["library_int8_src"] = "measured live: torch._int_mm 8192^3 (cuBLASLt INT8)"
     roofline = {"bound": W.dominant_bound, "kernel": W.dominant, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak,
-                "peak_src": peak_src,
+                "peak_src": peak_src, **extra,
                 "traffic": recorded_traffic(W.dominant),
                 "algorithmic_bytes_per_launch": dom["bytes"] / dom["launches"],
                 "algorithmic_flops_per_launch": dom["flops"] / dom["launches"],

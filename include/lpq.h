@@ -125,6 +125,15 @@ lpq_status lpq_quantize_act_int8(const uint16_t* X, int64_t M, int64_t K, int64_
 lpq_status lpq_quantize_weight_int8(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
                                     const float* smooth, int8_t* Wq, float* sw, void* stream);
 
+/* INT8 weight codes -> the E4M3 digit planes the tensor-core INT8 GEMM reads,
+ * for weights quantized once at load time: every code q = 16 h + l with
+ * h = floor(q / 16) in [-8, 7] and l in [0, 15], both exact in E4M3; planes
+ * [2][N][K] bytes (all h codes, then all l codes; rows of K, no padding).
+ * Pass planes as B with LPQ_GEMM_B_INT8_PLANES (the product stays the exact
+ * int32 one).  Wq: [N, ldw] int8, ldw a multiple of 16, K a multiple of 16. */
+lpq_status lpq_int8_weight_planes(const int8_t* Wq, int64_t N, int64_t K, int64_t ldw, uint8_t* planes,
+                                  void* stream);
+
 /* NVFP4: g = amax / (448 * 6) over the whole tensor (g = 1 if all zero);
  * per block of 16: c = E4M3((amax_b / 6) / g), s = dec(c) * g,
  * q = E2M1(x / s) (a block whose c is 0 stores zero codes).
@@ -166,6 +175,9 @@ size_t lpq_sf_offset(lpq_format fmt, int64_t rows, int64_t K, int64_t r, int64_t
  *       group, in fp32; Y = bf16(acc).  K % 128 == 0.
  *   fmt FP8, a_gran TENSOR_STATIC: sa[0] is the single activation scale.
  *   fmt INT8, ROW, ROW: acc exact in int32; Y = bf16((float(acc) * sa[m]) * sb[n]).
+ *       With a workspace of lpq_gemm_workspace_bytes (K <= 65536) the product
+ *       runs on the tcgen05 tensor cores through E4M3 digit planes (see
+ *       lpq_int8_weight_planes), else on the warp-level int8 MMA; same bits.
  *   fmt NVFP4: sa / sb are the scale-layout buffers of the quantizers; ga / gb
  *       point at the tensor scales g (gs + 1); Y = bf16(acc * ga * gb).
  *   fmt MXFP4: as NVFP4 without ga / gb.
@@ -213,6 +225,10 @@ typedef struct {
  * (lpq_gemm_workspace_bytes includes them; a missing or smaller workspace
  * returns LPQ_ERR_WORKSPACE).  Not accepted by lpq_gemm_scaled_noalloc. */
 #define LPQ_GEMM_A_BF16 2u
+/* flags: fmt INT8; B holds the planes of lpq_int8_weight_planes ([2][N][K],
+ * ldb ignored) instead of the int8 codes.  Needs a workspace of
+ * lpq_gemm_workspace_bytes (the activations' planes), else LPQ_ERR_WORKSPACE. */
+#define LPQ_GEMM_B_INT8_PLANES 4u
 
 size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d);
 lpq_status lpq_gemm_scaled(const lpq_gemm_desc* d, void* stream);

@@ -131,6 +131,13 @@ lpq_status gemm_int8(const lpq_gemm_desc* d, cudaStream_t st) {
   if (s != LPQ_OK) return s;
   LPQ_CHECK_NULL(d->sa);
   LPQ_CHECK_NULL(d->sb);
+  // with a workspace for the digit planes: the tcgen05 path
+  const bool planes = (d->flags & LPQ_GEMM_B_INT8_PLANES) != 0;
+  if (d->workspace && d->K <= kInt8TcMaxK && d->workspace_bytes >= int8_tc_workspace_bytes(d->M, d->N, d->K, planes))
+    return launch_int8_tc(static_cast<const int8_t*>(d->A), d->lda, d->B, d->ldb, planes, d->M, d->N, d->K,
+                          static_cast<const float*>(d->sa), static_cast<const float*>(d->sb), d->Y, d->ldy,
+                          d->workspace, st);
+  if (planes) return d->K <= kInt8TcMaxK ? LPQ_ERR_WORKSPACE : LPQ_ERR_SHAPE;   // planes need the tensor-core path
   CUtensorMap tmA, tmB;
   if ((s = make_tmap_u8(&tmA, d->A, d->M, d->K, d->lda, 128, 128, true)) != LPQ_OK) return s;
   if ((s = make_tmap_u8(&tmB, d->B, d->N, d->K, d->ldb, 128, 128, true)) != LPQ_OK) return s;
@@ -183,6 +190,8 @@ size_t lpq_gemm_workspace_bytes(const lpq_gemm_desc* d) {
   if (is_fp4(d)) {
     return plan_ws_bytes(plan_fp4(d->M, d->N, d->K, true, SIZE_MAX));
   }
+  if (is_int8(d))
+    return d->K <= kInt8TcMaxK ? int8_tc_workspace_bytes(d->M, d->N, d->K, (d->flags & LPQ_GEMM_B_INT8_PLANES) != 0) : 0;
   return 0;
 }
 

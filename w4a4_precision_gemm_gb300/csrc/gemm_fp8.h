@@ -59,6 +59,16 @@ constexpr int kFp8BlockBN = 256;
 lpq_status launch_fp8_block(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
                             const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
 
+// INT8 GEMM on the tcgen05 tensor cores through exact E4M3 digit planes
+// (gemm_int8_tc.cu): the planes of both operands live in a workspace of
+// int8_tc_workspace_bytes; K is limited so that every partial sum stays an
+// exact fp32 integer.
+constexpr int64_t kInt8TcMaxK = 65536;
+size_t int8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool b_planes);
+lpq_status launch_int8_tc(const int8_t* A, int64_t lda, const void* B, int64_t ldb, bool b_planes, int64_t M,
+                          int64_t N, int64_t K, const float* sx, const float* sw, uint16_t* Y, int64_t ldy, void* ws,
+                          cudaStream_t st);
+
 lpq_status launch_int8(const CUtensorMap& tmA, const CUtensorMap& tmB, int64_t M, int64_t N, int64_t K,
                        const float* sx, const float* sw, uint16_t* Y, int64_t ldy, cudaStream_t st);
 

@@ -24,6 +24,7 @@ GRAN_ROW, GRAN_BLOCK_1x128, GRAN_BLOCK_128x128, GRAN_TENSOR_STATIC = range(4)
 FMT_FP8, FMT_INT8, FMT_NVFP4, FMT_MXFP4 = range(4)
 GEMM_B_STATIC = 1
 GEMM_A_BF16 = 2
+GEMM_B_INT8_PLANES = 4
 
 EXPORTS = (
     "lpq_status_string", "lpq_last_cuda_error", "lpq_read_error_word", "lpq_clear_error_word",
@@ -31,7 +32,7 @@ EXPORTS = (
     "lpq_act_absmax_update", "lpq_smooth_calibrate",
     "lpq_quantize_act_fp8", "lpq_quantize_weight_fp8", "lpq_quantize_act_int8", "lpq_quantize_weight_int8",
     "lpq_quantize_act_nvfp4", "lpq_quantize_weight_nvfp4", "lpq_quantize_act_mxfp4", "lpq_quantize_weight_mxfp4",
-    "lpq_sf_bytes", "lpq_sf_offset", "lpq_gemm_workspace_bytes", "lpq_gemm_scaled",
+    "lpq_sf_bytes", "lpq_sf_offset", "lpq_gemm_workspace_bytes", "lpq_gemm_scaled", "lpq_int8_weight_planes",
 )
 
 
@@ -84,6 +85,7 @@ def _lib():
             "lpq_quantize_weight_fp8": (S, [P, I64, I64, I64, c_int, P, P, P]),
             "lpq_quantize_act_int8": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_weight_int8": (S, [P, I64, I64, I64, P, P, P, P]),
+            "lpq_int8_weight_planes": (S, [P, I64, I64, I64, P, P]),
             "lpq_quantize_act_nvfp4": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_weight_nvfp4": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_act_mxfp4": (S, [P, I64, I64, I64, P, P, P]),
@@ -160,6 +162,12 @@ def lpq_quantize_weight_int8(W, smooth, Wq, sw, stream=None):
     N, K, ld = _bf16_2d(W, "W")
     _check(_lib().lpq_quantize_weight_int8(_ptr(W), N, K, ld, _ptr(smooth), _ptr(Wq), _ptr(sw), _stream(stream)),
            "lpq_quantize_weight_int8")
+
+
+def lpq_int8_weight_planes(Wq, planes, stream=None):
+    N, K = Wq.shape
+    _check(_lib().lpq_int8_weight_planes(_ptr(Wq), N, K, int(Wq.stride(0)), _ptr(planes), _stream(stream)),
+           "lpq_int8_weight_planes")
 
 
 def lpq_quantize_act_nvfp4(X, Xq, sf, gs, stream=None):
@@ -281,6 +289,14 @@ def quantize_weight_int8(W, smooth=None, stream=None):
     sw = _empty((N,), torch.float32, W)
     lpq_quantize_weight_int8(W, smooth, Wq, sw, stream)
     return Wq, sw
+
+
+def int8_weight_planes(Wq, stream=None):
+    """[2, N, K] uint8: the E4M3 digit planes (high, low) of INT8 weight codes."""
+    N, K = Wq.shape
+    planes = _empty((2, N, K), torch.uint8, Wq)
+    lpq_int8_weight_planes(Wq, planes, stream)
+    return planes
 
 
 def quantize_nvfp4(X, stream=None):
