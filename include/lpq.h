@@ -71,6 +71,13 @@ int lpq_last_cuda_error(void);
  * (0 = none).  Synchronises the device; `lpq_clear_error_word` resets it. */
 lpq_status lpq_read_error_word(uint32_t* out);
 lpq_status lpq_clear_error_word(void);
+/* Diagnostics for the failure path: one kernel waits, as every barrier wait
+ * in the library's kernels does, on a barrier that nothing completes; after
+ * limit_ns (1 .. 2e9) it gives up, writes LPQ_SELFTEST_WAIT_CODE into the
+ * device error word (if it was 0) and returns.  No trap and no fault: the
+ * context stays usable.  Asynchronous on `stream`. */
+#define LPQ_SELFTEST_WAIT_CODE 0x0F0Fu
+lpq_status lpq_selftest_bounded_wait(uint64_t limit_ns, void* stream);
 /* Library version and the number of kernels launched by this host thread
  * since the last reset (for launch accounting). */
 const char* lpq_version(void);

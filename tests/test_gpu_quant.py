@@ -250,3 +250,20 @@ def test_invalid_arguments_rejected_on_host():
 def ctypes_ptr_plus(t, nbytes):
     import ctypes
     return ctypes.c_void_p(t.data_ptr() + nbytes)
+
+
+def test_bounded_wait_records_timeout_and_context_survives():
+    """The failure path of every kernel wait, made to run out on purpose: a
+    barrier nothing completes, a 50 ms limit.  The kernel records its code in
+    the device error word and returns; the context keeps working."""
+    L = lpq()
+    L.lpq_clear_error_word()
+    L.lpq_selftest_bounded_wait(50_000_000)
+    torch.cuda.synchronize()
+    assert L.lpq_read_error_word() == L.LPQ_SELFTEST_WAIT_CODE
+    L.lpq_clear_error_word()
+    # the same context still runs the path
+    X = torch.ones((4, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = L.quantize_act_fp8(X, L.GRAN_ROW)
+    torch.cuda.synchronize()
+    assert torch.all(s == s[0]) and L.lpq_read_error_word() == 0

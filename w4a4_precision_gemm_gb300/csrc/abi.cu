@@ -13,6 +13,7 @@
 #include "../../include/lpq.h"
 #include "gemm_fp8.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace lpq {
 
@@ -106,7 +107,42 @@ lpq_status make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_
 
 using namespace lpq;
 
+namespace lpq_diag {
+
+// One barrier wait that nothing ends, bounded the way every wait in the
+// library's kernels is: after limit_ns the thread records `where` in the
+// device error word and the kernel returns (no trap; the context stays usable).
+__global__ void bounded_wait_kernel(uint64_t limit_ns, uint32_t* err, uint32_t where) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    lpq::mbar_init(lpq::smem_u32(&bar), 1);
+    lpq::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = lpq::globaltimer_ns();
+    while (!lpq::mbar_try_wait(lpq::smem_u32(&bar), 0)) {
+      if (lpq::globaltimer_ns() - t0 > limit_ns) {
+        atomicCAS(err, 0u, where);
+        break;
+      }
+    }
+  }
+}
+
+}  // namespace lpq_diag
+
 extern "C" {
+
+lpq_status lpq_selftest_bounded_wait(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return LPQ_ERR_SHAPE;
+  uint32_t* err = error_word_ptr();
+  if (!err) return record_cuda(cudaErrorInvalidSymbol);
+  lpq_diag::bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, err, LPQ_SELFTEST_WAIT_CODE);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LPQ_OK : record_cuda(e);
+}
+
 
 const char* lpq_status_string(lpq_status s) {
   switch (s) {

@@ -33,6 +33,7 @@ EXPORTS = (
     "lpq_quantize_act_fp8", "lpq_quantize_weight_fp8", "lpq_quantize_act_int8", "lpq_quantize_weight_int8",
     "lpq_quantize_act_nvfp4", "lpq_quantize_weight_nvfp4", "lpq_quantize_act_mxfp4", "lpq_quantize_weight_mxfp4",
     "lpq_sf_bytes", "lpq_sf_offset", "lpq_gemm_workspace_bytes", "lpq_gemm_scaled", "lpq_int8_weight_planes",
+    "lpq_selftest_bounded_wait",
 )
 
 
@@ -86,6 +87,7 @@ def _lib():
             "lpq_quantize_act_int8": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_weight_int8": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_int8_weight_planes": (S, [P, I64, I64, I64, P, P]),
+            "lpq_selftest_bounded_wait": (S, [ctypes.c_uint64, P]),
             "lpq_quantize_act_nvfp4": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_weight_nvfp4": (S, [P, I64, I64, I64, P, P, P, P]),
             "lpq_quantize_act_mxfp4": (S, [P, I64, I64, I64, P, P, P]),
@@ -229,6 +231,13 @@ def lpq_gemm_workspace_bytes(desc):
 
 def lpq_gemm_scaled(desc, stream=None):
     _check(_lib().lpq_gemm_scaled(ctypes.byref(desc), _stream(stream)), "lpq_gemm_scaled")
+
+
+LPQ_SELFTEST_WAIT_CODE = 0x0F0F
+
+
+def lpq_selftest_bounded_wait(limit_ns, stream=None):
+    _check(_lib().lpq_selftest_bounded_wait(int(limit_ns), _stream(stream)), "lpq_selftest_bounded_wait")
 
 
 def lpq_read_error_word():
