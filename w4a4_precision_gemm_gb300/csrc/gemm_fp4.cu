@@ -10,10 +10,16 @@
 // Same warp roles as the FP8 kernel.  Per pipeline stage the producer loads a
 // 128 x 256 (A) and BN x 256 (B) tile of packed nibbles (one 128-byte
 // swizzled row each) plus the matching scale-factor tiles (512-byte blocks of
-// 128 rows x 4 scales, the layout the quantizers write) with bulk copies.  The
-// MMA thread moves the scales into a per-stage tensor-memory slot with
-// tcgen05.cp (32 lanes x 16 bytes, replicated to the four lane quarters) and
-// issues four K=64 block-scaled MMAs.
+// 128 rows x 4 scales, the layout the quantizers write) with bulk copies.
+// The block-scaled MMA reads the scales of A row m from tensor-memory lane m,
+// column (slot + m / 32), and the scales of B row n from every lane quarter
+// (lane n % 32 of the quarter, column slot + 4 (n / 128) + (n % 128) / 32): in
+// each quarter lane i, column 4 g + c holds row 128 g + 32 c + i, i.e. every
+// 512-byte atom replicated into the four quarters.  The four epilogue warps
+// (one per lane quarter, idle during the K loop) write that layout with
+// tcgen05.st from shared memory, so the MMA thread issues nothing but the
+// four K=64 block-scaled MMAs of a stage: a tcgen05.cp of each atom, issued
+// by the MMA thread, took about as long as the MMAs themselves.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -73,6 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int64_t sf_kb4,
                     const GemmParams p) {
   using C = Fp4Cfg<BN, NV>;
+  static_assert(BN == 256 && C::kAtomsPerStage % 2 == 0, "scale staging assumes two B groups, atom pairs");
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSFA = sB + S * BN * kBKBytes;
   uint8_t* sSFB = sSFA + S * C::kSfaBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + S * C::kSfbBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -91,11 +98,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull = [&](int a) { return smem_u32(bars + 2 * S + a); };
   auto tempty = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
   const uint32_t drain = smem_u32(bars + 2 * S + 4);
+  auto sfr = [&](int s) { return smem_u32(bars + 2 * S + 5 + s); };   // scales of stage s in tensor memory
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
+      mbar_init(sfr(s), 4);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
@@ -175,20 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(full(stage), phase, p.err, 0x203u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(sfr(stage), phase, p.err, 0x206u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int ksteps = min(4, ksteps_total - kb * 4);
-          const int atoms = NV ? ksteps : (ksteps + 1) / 2;
           const uint32_t tsfa = sf_base + stage * (C::kSfaCols + C::kSfbCols);
           const uint32_t tsfb = tsfa + C::kSfaCols;
-          // scales: smem -> tensor memory (4 columns per 512-byte atom)
-          for (int a = 0; a < atoms; ++a) {
-            tc_cp_32x128b_warpx4(tsfa + a * 4, smem_desc(smem_u32(sSFA + stage * C::kSfaBytes + a * kAtom), 16, 128, 0));
-#pragma unroll
-            for (int g = 0; g < C::kBGroups; ++g)
-              tc_cp_32x128b_warpx4(tsfb + (a * C::kBGroups + g) * 4,
-                                   smem_desc(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes + a * kAtom), 16,
-                                             128, 0));
-          }
           const uint32_t a0 = smem_u32(sA + stage * kBM * kBKBytes);
           const uint32_t b0 = smem_u32(sB + stage * BN * kBKBytes);
           for (int k = 0; k < ksteps; ++k) {
@@ -216,10 +216,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int quarter = warp & 3;
-    uint32_t acc = 0, acc_phase = 0;
+    // this warp's lane quarter of the per-stage scale slots
+    const uint32_t sf_lanes = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kAccBufs * BN;
+    uint32_t acc = 0, acc_phase = 0, stage = 0, phase = 0;
+    bool ok = true;
     WorkIter wi(p, blockIdx.x, gridDim.x);
     Seg w;
-    while (wi.next(p, blockIdx.x, gridDim.x, w)) {
+    while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if (!warp_wait(full(stage), phase, p.err, 0x205u, abort_flag)) { ok = false; break; }
+        // atom a of A -> columns 4a..4a+3; atom a of B group g -> columns 8a + 4g..+3
+        // (lane i gets bytes 16 i..16 i + 15 of the atom); atoms past the end
+        // of K were not loaded and are never read by an MMA
+        const uint32_t tsfa = sf_lanes + stage * (C::kSfaCols + C::kSfbCols);
+        const uint32_t tsfb = tsfa + C::kSfaCols;
+        const uint8_t* a_src = sSFA + stage * C::kSfaBytes + lane * 16;
+        const uint8_t* b_src = sSFB + stage * C::kSfbBytes + lane * 16;
+#pragma unroll
+        for (int a = 0; a < C::kAtomsPerStage; a += 2)
+          tmem_st_32x32b_x8(tsfa + a * 4, *reinterpret_cast<const uint4*>(a_src + a * kAtom),
+                            *reinterpret_cast<const uint4*>(a_src + (a + 1) * kAtom));
+#pragma unroll
+        for (int a = 0; a < C::kAtomsPerStage; ++a)
+          tmem_st_32x32b_x8(tsfb + a * 8, *reinterpret_cast<const uint4*>(b_src + a * kAtom),
+                            *reinterpret_cast<const uint4*>(b_src + C::kSfaBytes + a * kAtom));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfr(stage));
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
       if (!warp_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
       tc_fence_after();
       epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
