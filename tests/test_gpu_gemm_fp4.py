@@ -50,7 +50,8 @@ def _gpu_gemm(L, fmt, ox, ow, M, N, K, workspace=False):
     return bf16_to_f64(host(Y))
 
 
-SHAPES = [(128, 128, 256), (1, 128, 64), (130, 200, 96), (512, 1024, 8192), (300, 640, 1056), (64, 8192, 2048)]
+SHAPES = [(128, 128, 256), (1, 128, 64), (130, 200, 96), (512, 1024, 8192), (300, 640, 1056), (64, 8192, 2048),
+          (96, 104, 256), (64, 24, 128)]   # a clipped last 32-column block; Y narrower than 32 columns
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])

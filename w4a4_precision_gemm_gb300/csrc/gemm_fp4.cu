@@ -73,6 +73,55 @@ static_assert(Fp4Cfg<128, true>::kNeedCols <= 512, "tensor memory budget");
 static_assert(Fp4Cfg<256, true>::kNeedCols <= 512 && Fp4Cfg<256, false>::kNeedCols <= 512, "tensor memory budget");
 static_assert(Fp4Cfg<256, true>::kSmemBytes <= 227 * 1024, "shared memory budget");
 
+// Epilogue of a whole tile that frees tensor memory before it writes Y: each
+// lane converts its row of the 128 x BN accumulator, y = acc * (g_x g_w)
+// (NVFP4) or acc (MXFP4), into BN / 2 registers of packed bf16, the warp
+// releases the accumulator (arrives on `tempty`), and only then stores the
+// row, so the next tile's MMAs run under the stores.  (With one accumulator
+// per CTA the MMAs otherwise wait for the stores, and the CTAs, which finish
+// tiles at about the same time, all store at once.)
+template <int BN>
+__device__ __forceinline__ void epilogue_tile_release_first(const GemmParams& p, const Seg& w, uint32_t tmem_acc,
+                                                            int quarter, int lane, uint32_t tempty_bar) {
+  const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int i = w.i_tile * 128 + quarter * 32 + lane;
+  const bool scaled = p.gx != nullptr;
+  const float g = scaled ? __fmul_rn(__ldg(p.gx), __ldg(p.gw)) : 1.0f;
+  uint32_t y[BN / 2];
+#pragma unroll
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int t = 0; t < 32; t += 2) {
+      const float a = __uint_as_float(r[t]), b = __uint_as_float(r[t + 1]);
+      y[(c + t) / 2] = scaled ? pack_bf16x2(__fmul_rn(a, g), __fmul_rn(b, g)) : pack_bf16x2(a, b);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty_bar);
+  if (i >= p.I) return;
+  const int jt = w.j_tile * BN;
+  uint16_t* yrow = p.Y + static_cast<int64_t>(i) * p.ldy + jt;
+  const int n = p.J - jt;   // columns of this tile inside Y
+  if (n >= BN) {
+#pragma unroll
+    for (int c = 0; c < BN; c += 8)
+      *reinterpret_cast<uint4*>(yrow + c) = make_uint4(y[c / 2], y[c / 2 + 1], y[c / 2 + 2], y[c / 2 + 3]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < BN; c += 2) {
+      if (c + 1 < n) {
+        *reinterpret_cast<uint32_t*>(yrow + c) = y[c / 2];
+      } else if (c < n) {
+        yrow[c] = static_cast<uint16_t>(y[c / 2]);
+      }
+    }
+  }
+}
+
 template <int BN, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -249,10 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!warp_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
       tc_fence_after();
-      epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
+      if (w.full) {
+        epilogue_tile_release_first<BN>(p, w, tmem_base + acc * BN, quarter, lane, tempty(acc));
+      } else {
+        epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+      }
       if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
   }
