@@ -15,11 +15,12 @@
 // column (slot + m / 32), and the scales of B row n from every lane quarter
 // (lane n % 32 of the quarter, column slot + 4 (n / 128) + (n % 128) / 32): in
 // each quarter lane i, column 4 g + c holds row 128 g + 32 c + i, i.e. every
-// 512-byte atom replicated into the four quarters.  The four epilogue warps
-// (one per lane quarter, idle during the K loop) write that layout with
-// tcgen05.st from shared memory, so the MMA thread issues nothing but the
-// four K=64 block-scaled MMAs of a stage: a tcgen05.cp of each atom, issued
-// by the MMA thread, took about as long as the MMAs themselves.
+// 512-byte atom replicated into the four quarters.  Four scale-staging warps
+// (one per lane quarter) write that layout with tcgen05.st from shared
+// memory, so the MMA thread issues nothing but the four K=64 block-scaled
+// MMAs of a stage: a tcgen05.cp of each atom, issued by the MMA thread, took
+// about as long as the MMAs themselves.  (Staging them in the epilogue warps
+// instead stalled the next tile's MMAs behind the previous tile's stores.)
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -32,7 +33,7 @@
 namespace lpq {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;      // TMA, MMA, 4 epilogue warps, 4 scale-staging warps
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;        // 256 packed E2M1 elements per row per stage
 constexpr int kKPerStage = 256;
@@ -122,8 +123,10 @@ __device__ __forceinline__ void epilogue_tile_release_first(const GemmParams& p,
   }
 }
 
+// 10 warps put three on two SM sub-partitions, whose register file holds 16K
+// registers: 168 per thread is the most this block can launch with.
 template <int BN, bool NV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(168)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int64_t sf_kb4,
                     const GemmParams p) {
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSFA = sB + S * BN * kBKBytes;
   uint8_t* sSFB = sSFA + S * C::kSfaBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + S * C::kSfbBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -148,12 +151,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
   const uint32_t drain = smem_u32(bars + 2 * S + 4);
   auto sfr = [&](int s) { return smem_u32(bars + 2 * S + 5 + s); };   // scales of stage s in tensor memory
+  auto sff = [&](int s) { return smem_u32(bars + 3 * S + 5 + s); };   // scales of stage s in shared memory
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
       mbar_init(sfr(s), 4);
+      mbar_init(sff(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
@@ -198,17 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf_bytes = atoms * kAtom;
           // 128-row groups of this B tile that exist in the scale buffer
           const int bgroups = min(C::kBGroups, (p.J + 127) / 128 - w.j_tile * C::kBGroups);
-          mbar_arrive_expect_tx(full(stage), (kBM + BN) * kBKBytes + sf_bytes * (1 + bgroups));
-          tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
-          tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
+          // the scale tiles first, on their own barrier: the staging warps
+          // move them into tensor memory while the operand tiles are in flight
           const int64_t atom0 = static_cast<int64_t>(kb) * C::kAtomsPerStage;
+          mbar_arrive_expect_tx(sff(stage), sf_bytes * (1 + bgroups));
           bulk_g2s(smem_u32(sSFA + stage * C::kSfaBytes), sfa + (w.i_tile * sf_kb4 + atom0) * kAtom, sf_bytes,
-                   full(stage));
+                   sff(stage));
 #pragma unroll
           for (int g = 0; g < C::kBGroups; ++g)
             if (g < bgroups)
               bulk_g2s(smem_u32(sSFB + stage * C::kSfbBytes + g * C::kSfaBytes),
-                     sfb + ((w.j_tile * C::kBGroups + g) * sf_kb4 + atom0) * kAtom, sf_bytes, full(stage));
+                     sfb + ((w.j_tile * C::kBGroups + g) * sf_kb4 + atom0) * kAtom, sf_bytes, sff(stage));
+          mbar_arrive_expect_tx(full(stage), (kBM + BN) * kBKBytes);
+          tma_load_2d(smem_u32(sA + stage * kBM * kBKBytes), &tmA, full(stage), kb * kBKBytes, w.i_tile * kBM, pol_a);
+          tma_load_2d(smem_u32(sB + stage * BN * kBKBytes), &tmB, full(stage), kb * kBKBytes, w.j_tile * BN, pol_b);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -217,7 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         volatile int no_abort = 0;
         for (int s = 0; s < S; ++s)
-          if (issued & (1u << s)) mbar_wait(full(s), (issued_par >> s) & 1u, nullptr, 0, &no_abort);
+          if (issued & (1u << s)) {
+            mbar_wait(sff(s), (issued_par >> s) & 1u, nullptr, 0, &no_abort);
+            mbar_wait(full(s), (issued_par >> s) & 1u, nullptr, 0, &no_abort);
+          }
       }
     }
   } else if (warp == 1) {
@@ -263,17 +274,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       mbar_wait(drain, 0, nullptr, 0, &no_abort);
     }
-  } else {
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    // this warp's lane quarter of the per-stage scale slots
+    uint32_t acc = 0, acc_phase = 0;
+    WorkIter wi(p, blockIdx.x, gridDim.x);
+    Seg w;
+    while (wi.next(p, blockIdx.x, gridDim.x, w)) {
+      if (!warp_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
+      tc_fence_after();
+      if (w.full) {
+        epilogue_tile_release_first<BN>(p, w, tmem_base + acc * BN, quarter, lane, tempty(acc));
+      } else {
+        epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+      }
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+    }
+  } else {
+    // ------------------------------------------------------ scale staging
+    // warps 6..9, one per lane quarter: every stage's scale tiles from shared
+    // memory into this warp's quarter of the stage's tensor-memory slot
+    const int quarter = warp & 3;
     const uint32_t sf_lanes = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kAccBufs * BN;
-    uint32_t acc = 0, acc_phase = 0, stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0;
     bool ok = true;
     WorkIter wi(p, blockIdx.x, gridDim.x);
     Seg w;
     while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (!warp_wait(full(stage), phase, p.err, 0x205u, abort_flag)) { ok = false; break; }
+        if (!warp_wait(sff(stage), phase, p.err, 0x205u, abort_flag)) { ok = false; break; }
         // atom a of A -> columns 4a..4a+3; atom a of B group g -> columns 8a + 4g..+3
         // (lane i gets bytes 16 i..16 i + 15 of the atom); atoms past the end
         // of K were not loaded and are never read by an MMA
@@ -295,18 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(sfr(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) break;
-      if (!warp_wait(tfull(acc), acc_phase, p.err, 0x204u, abort_flag)) break;
-      tc_fence_after();
-      if (w.full) {
-        epilogue_tile_release_first<BN>(p, w, tmem_base + acc * BN, quarter, lane, tempty(acc));
-      } else {
-        epilogue_tile<BN>(p, w, tmem_base + acc * BN, quarter, lane);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(acc));
-      }
-      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
