@@ -30,6 +30,14 @@
 namespace lpq {
 namespace {
 
+// Read-only load kept in program order (volatile asm): the epilogue loads a
+// chunk's weight scales where it uses them instead of all 128 up front.
+__device__ __forceinline__ float ld_nc_ordered(const float* ptr) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+  return v;
+}
+
 constexpr int kThreads = 192;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
@@ -203,26 +211,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
       const int i = w.i_tile * kBM + row_in_tile;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t hh[32], mid[32], ll[32];
-        tmem_ld_32x32b_x32(tmem_base + lanes + c0, hh);
-        tmem_ld_32x32b_x32(tmem_base + lanes + kBN + c0, mid);
-        tmem_ld_32x32b_x32(tmem_base + lanes + 2 * kBN + c0, ll);
-        tmem_ld_wait();
-        float v[32];
+      const int jt = w.j_tile * kBN;
+      const float sxi = i < p.I ? __ldg(p.sx + i) : 0.0f;
+      // the whole row into packed bf16 first, y = bf16((float(acc) s_x) s_w),
+      // then release the accumulators and store: the next tile's MMAs run
+      // under the stores (three accumulators leave no room for a second set)
+      uint32_t y[kBN / 2];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int acc = 256 * __float2int_rn(__uint_as_float(hh[j])) + 16 * __float2int_rn(__uint_as_float(mid[j])) +
-                          __float2int_rn(__uint_as_float(ll[j]));
-          v[j] = static_cast<float>(acc);
+      for (int c0 = 0; c0 < kBN; c0 += 16) {
+        uint32_t hh[16], mid[16], ll[16];
+        tmem_ld_32x32b_x16(tmem_base + lanes + c0, hh);
+        tmem_ld_32x32b_x16(tmem_base + lanes + kBN + c0, mid);
+        tmem_ld_32x32b_x16(tmem_base + lanes + 2 * kBN + c0, ll);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          float yv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int acc = 256 * __float2int_rn(__uint_as_float(hh[j + e])) +
+                            16 * __float2int_rn(__uint_as_float(mid[j + e])) + __float2int_rn(__uint_as_float(ll[j + e]));
+            const int jj = jt + c0 + j + e;
+            const float swj = jj < p.J ? ld_nc_ordered(p.sw + jj) : 0.0f;
+            yv[e] = __fmul_rn(__fmul_rn(static_cast<float>(acc), sxi), swj);
+          }
+          y[(c0 + j) / 2] = pack_bf16x2(yv[0], yv[1]);
         }
-        epilogue_store<32>(p, i, w.j_tile * kBN + c0, v);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
       tphase ^= 1u;
+      if (i < p.I) {
+        uint16_t* yrow = p.Y + static_cast<int64_t>(i) * p.ldy + jt;
+        const int n = p.J - jt;   // columns of this tile inside Y
+        if (n >= kBN) {
+#pragma unroll
+          for (int c = 0; c < kBN; c += 8)
+            *reinterpret_cast<uint4*>(yrow + c) = make_uint4(y[c / 2], y[c / 2 + 1], y[c / 2 + 2], y[c / 2 + 3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; c += 2) {
+            if (c + 1 < n) {
+              *reinterpret_cast<uint32_t*>(yrow + c) = y[c / 2];
+            } else if (c < n) {
+              yrow[c] = static_cast<uint16_t>(y[c / 2]);
+            }
+          }
+        }
+      }
     }
   }
 
