@@ -21,6 +21,9 @@
 // MMAs of a stage: a tcgen05.cp of each atom, issued by the MMA thread, took
 // about as long as the MMAs themselves.  (Staging them in the epilogue warps
 // instead stalled the next tile's MMAs behind the previous tile's stores.)
+// The staging warps arrive on the stage's full barrier (count 1 + 4), so the
+// MMA thread waits once per stage: its per-stage bookkeeping sits on the
+// critical path of the 4-stage ring.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -140,7 +143,7 @@ __global__ void __maxnreg__(168)
   uint8_t* sSFA = sB + S * BN * kBKBytes;
   uint8_t* sSFB = sSFA + S * C::kSfaBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + S * C::kSfbBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * S + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -150,14 +153,14 @@ __global__ void __maxnreg__(168)
   auto tfull = [&](int a) { return smem_u32(bars + 2 * S + a); };
   auto tempty = [&](int a) { return smem_u32(bars + 2 * S + 2 + a); };
   const uint32_t drain = smem_u32(bars + 2 * S + 4);
-  auto sfr = [&](int s) { return smem_u32(bars + 2 * S + 5 + s); };   // scales of stage s in tensor memory
-  auto sff = [&](int s) { return smem_u32(bars + 3 * S + 5 + s); };   // scales of stage s in shared memory
+  // full[s] completes when the operand tiles have landed (TMA bytes) and the
+  // four staging warps have put the stage's scales into tensor memory
+  auto sff = [&](int s) { return smem_u32(bars + 2 * S + 5 + s); };   // scales of stage s in shared memory
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), 1 + 4);
       mbar_init(empty(s), 1);
-      mbar_init(sfr(s), 4);
       mbar_init(sff(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -244,14 +247,15 @@ __global__ void __maxnreg__(168)
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(full(stage), phase, p.err, 0x203u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(sfr(stage), phase, p.err, 0x206u, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int ksteps = min(4, ksteps_total - kb * 4);
           const uint32_t tsfa = sf_base + stage * (C::kSfaCols + C::kSfbCols);
           const uint32_t tsfb = tsfa + C::kSfaCols;
           const uint32_t a0 = smem_u32(sA + stage * kBM * kBKBytes);
           const uint32_t b0 = smem_u32(sB + stage * BN * kBKBytes);
-          for (int k = 0; k < ksteps; ++k) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (k >= ksteps) break;
             const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, 2);
             const uint32_t acc_in = (kb > w.kb0 || k > 0) ? 1u : 0u;
@@ -324,7 +328,7 @@ __global__ void __maxnreg__(168)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfr(stage));
+        if (lane == 0) mbar_arrive(full(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
