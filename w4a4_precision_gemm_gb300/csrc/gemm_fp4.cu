@@ -239,6 +239,20 @@ __global__ void __maxnreg__(168)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t sf_base = tmem_base + C::kAccBufs * BN;
+      // operand descriptors of stage 0; a stage / a K step moves the start
+      // address (bytes >> 4, 14 bits, shared memory stays below 256 KB)
+      const uint64_t ad0 = smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint64_t bd0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      constexpr uint64_t kAStage = (kBM * kBKBytes) >> 4, kBStage = (BN * kBKBytes) >> 4, kKStep = 32 >> 4;
+      auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t tsfa, uint32_t tsfb, int k, uint32_t acc_in) {
+        if constexpr (NV) {
+          mma_nvf4(d, ad + k * kKStep, bd + k * kKStep, C::kIdesc, tsfa + k * 4, tsfb + k * 4 * C::kBGroups, acc_in);
+        } else {
+          const uint32_t id = static_cast<uint32_t>((k & 1) * 2);
+          mma_mxf4(d, ad + k * kKStep, bd + k * kKStep, C::kIdesc | (id << 4) | (id << 29), tsfa + (k >> 1) * 4,
+                   tsfb + (k >> 1) * 4 * C::kBGroups, acc_in);
+        }
+      };
       WorkIter wi(p, blockIdx.x, gridDim.x);
       Seg w;
       while (ok && wi.next(p, blockIdx.x, gridDim.x, w)) {
@@ -248,24 +262,19 @@ __global__ void __maxnreg__(168)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(full(stage), phase, p.err, 0x203u, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const int ksteps = min(4, ksteps_total - kb * 4);
           const uint32_t tsfa = sf_base + stage * (C::kSfaCols + C::kSfbCols);
           const uint32_t tsfb = tsfa + C::kSfaCols;
-          const uint32_t a0 = smem_u32(sA + stage * kBM * kBKBytes);
-          const uint32_t b0 = smem_u32(sB + stage * BN * kBKBytes);
+          const uint64_t ad = ad0 + stage * kAStage, bd = bd0 + stage * kBStage;
+          const uint32_t first = kb > w.kb0 ? 1u : 0u;
+          if (kb * 4 + 4 <= ksteps_total) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (k >= ksteps) break;
-            const uint64_t ad = smem_desc(a0 + k * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b0 + k * 32, 16, 1024, 2);
-            const uint32_t acc_in = (kb > w.kb0 || k > 0) ? 1u : 0u;
-            if constexpr (NV) {
-              mma_nvf4(d, ad, bd, C::kIdesc, tsfa + k * 4, tsfb + k * 4 * C::kBGroups, acc_in);
-            } else {
-              const uint32_t id = static_cast<uint32_t>((k & 1) * 2);
-              const uint32_t idesc = C::kIdesc | (id << 4) | (id << 29);
-              mma_mxf4(d, ad, bd, idesc, tsfa + (k >> 1) * 4, tsfb + (k >> 1) * 4 * C::kBGroups, acc_in);
-            }
+            for (int k = 0; k < 4; ++k) mma(d, ad, bd, tsfa, tsfb, k, k > 0 ? 1u : first);
+          } else {
+            // last stage of a K not a multiple of 256: fewer K steps
+            const int ksteps = ksteps_total - kb * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k < ksteps) mma(d, ad, bd, tsfa, tsfb, k, k > 0 ? 1u : first);
           }
           tc_commit(empty(stage));
           if (++stage == S) { stage = 0; phase ^= 1u; }
