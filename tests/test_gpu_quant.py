@@ -52,6 +52,45 @@ def test_fp8_every_bf16_value():
     assert np.array_equal(host(q2), Q.fp8_static(_f32(b), np.float32(0.37)))
 
 
+def _many_scales(M, K, seed):
+    """Rows whose magnitudes span 2^-40 .. 2^40 (a different divisor per row, per
+    1x128 group and per 16-block), some rows holding small integer multiples of
+    a power of two so that many quotients are exact or sit on rounding ties."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    e = g.integers(-40, 41, size=(M, 1)).astype(np.float64)
+    x = g.standard_normal((M, K)) * np.exp2(e)
+    ints = g.integers(-448, 449, size=(M, K)).astype(np.float64) * np.exp2(e - 6)
+    pick = (np.arange(M) % 3 == 1)[:, None]
+    x = np.where(pick, ints, x).astype(np.float32)
+    return synth.bf16_bits_from_f32(x)
+
+
+def test_shared_divisor_quantizers_many_scales():
+    """Codes of every quantizer whose divisor is shared by a row, a 1x128 group
+    or a 16-element block (FP8 per token, FP8 1x128, INT8, NVFP4), over 2048
+    rows with different magnitudes: each code must equal the oracle's, which
+    divides exactly."""
+    L = lpq()
+    M, K = 2048, 1024
+    xb = _many_scales(M, K, 77)
+    xf = _f32(xb)
+    X = dev_bf16(xb)
+    q, s = L.quantize_act_fp8(X, L.GRAN_ROW)
+    qo, so = Q.fp8_per_row(xf)
+    assert np.array_equal(host(s), so) and np.array_equal(host(q), qo)
+    q, s = L.quantize_act_fp8(X, L.GRAN_BLOCK_1x128)
+    qo, so = Q.fp8_per_group_1x128(xf)
+    assert np.array_equal(host(q), qo) and np.array_equal(host(s).reshape(K // 128, M).T, so)
+    q, s = L.quantize_act_int8(X, None)
+    qo, so = Q.int8_per_row(xf)
+    assert np.array_equal(host(s), so) and np.array_equal(host(q), qo)
+    q, sf, gs = L.quantize_nvfp4(X)
+    qo, sfo, amax, gg = Q.nvfp4(xf)
+    assert host(gs)[1] == gg
+    assert np.array_equal(unpack_nibbles(host(q)), qo)
+    assert np.array_equal(sf_to_logical(L, L.FMT_NVFP4, host(sf), M, K, 16), sfo)
+
+
 @pytest.mark.parametrize("M,K", [(1, 128), (7, 4096), (130, 14336)])
 def test_fp8_1x128(M, K):
     L = lpq()
