@@ -244,6 +244,42 @@ class Workload:
         t = self.torch
         return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).cuda()
 
+    def arena(self, wl):
+        """One device buffer (and its pinned host mirror) for all of a step's
+        activations and one for all its outputs: the end-to-end step moves
+        each with a single copy.  `input` / `output` hand out [rows, cols]
+        views in call order (offsets stay 16-byte aligned: K, N % 8 == 0)."""
+        t = self.torch
+        n_in = sum(M * K for M in wl.Ms for K, _ in wl.KNs)
+        n_out = sum(M * N for M in wl.Ms for _, N in wl.KNs)
+        self.din = t.empty(n_in, dtype=t.bfloat16, device="cuda")
+        self.dout = t.empty(n_out, dtype=t.bfloat16, device="cuda")
+        self.hin = t.empty(n_in, dtype=t.bfloat16).pin_memory()
+        self.hout = t.empty(n_out, dtype=t.bfloat16).pin_memory()
+        self._oi = self._oo = 0
+        self.dev_in, self.dev_out, self.host_in, self.host_out = [], [], [], []
+        self.subset = False
+
+    def input(self, bits):
+        t = self.torch
+        M, K = bits.shape
+        h = self.hin[self._oi:self._oi + M * K].view(M, K)
+        h.copy_(t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16))
+        d = self.din[self._oi:self._oi + M * K].view(M, K)
+        d.copy_(h)
+        self._oi += M * K
+        self.host_in.append(h)
+        self.dev_in.append(d)
+        return d
+
+    def output(self, M, N):
+        h = self.hout[self._oo:self._oo + M * N].view(M, N)
+        d = self.dout[self._oo:self._oo + M * N].view(M, N)
+        self._oo += M * N
+        self.host_out.append(h)
+        self.dev_out.append(d)
+        return d
+
 
 def workload_config(name: str) -> dict:
     """The `config` object of a workload's JSON line (no device needed: the
@@ -276,7 +312,7 @@ def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
     W.config = workload_config("decode_fp8")
     W.dominant = "gemm_fp8"
     W.dominant_bound = "hbm"
-    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    W.arena(wl)
     for mi, M in enumerate(wl.Ms):
         for si, (K, N) in enumerate(wl.KNs):
             wb = CFG.make_w(wl, N, K, salt=si)              # same weights, one fp8 copy per M
@@ -284,10 +320,10 @@ def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
             Wq, sw = L.quantize_weight_fp8(Wd, L.GRAN_ROW)
             del Wd
             xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
-            Xd = W.dev_bf16(xb)
+            Xd = W.input(xb)
             Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
             sx = torch.empty((M,), dtype=torch.float32, device="cuda")
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            Y = W.output(M, N)
             ws = L.workspace_for(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
             desc = L.make_desc(L.FMT_FP8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws,
                                flags=L.GEMM_B_STATIC)   # weights quantized at load time
@@ -297,10 +333,6 @@ def build_decode_fp8(L, torch, wl=CFG.DECODE_FP8):
                                 bytes=M * K * 2 + M * K + 4 * M, flops=0))
             W.calls.append(dict(kind="gemm_fp8", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
                                 bytes=N * K + 4 * N + M * K + 4 * M + 2 * M * N, flops=2 * M * N * K))
-            W.dev_in.append(Xd)
-            W.dev_out.append(Y)
-            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
-            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
     return W
 
 
@@ -311,7 +343,7 @@ def build_fp4(L, torch, wl):
     W.dominant = "gemm_fp4"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "fp4"
-    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    W.arena(wl)
     F = L.FMT_NVFP4 if nv else L.FMT_MXFP4
     for mi, M in enumerate(wl.Ms):
         for si, (K, N) in enumerate(wl.KNs):
@@ -322,11 +354,11 @@ def build_fp4(L, torch, wl):
                 (Wq, sfw), gsw = L.quantize_mxfp4(Wd), None
             del Wd
             xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
-            Xd = W.dev_bf16(xb)
+            Xd = W.input(xb)
             Xq = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
             sfx = torch.empty((L.lpq_sf_bytes(F, M, K),), dtype=torch.uint8, device="cuda")
             gsx = torch.empty((2,), dtype=torch.float32, device="cuda")
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            Y = W.output(M, N)
             ws = L.workspace_for(F, L.GRAN_ROW, L.GRAN_ROW, M, N, K)
             desc = L.make_desc(F, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sfx, sfw, Y, M=M, N=N, K=K,
                                ga=gsx[1:] if nv else None, gb=gsw[1:] if nv else None, workspace=ws)
@@ -340,10 +372,6 @@ def build_fp4(L, torch, wl):
                                 bytes=M * K * 2 + M * K // 2 + M * K // blk, flops=0))
             W.calls.append(dict(kind="gemm_fp4", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
                                 bytes=(M + N) * K // 2 + (M + N) * K // blk + 2 * M * N, flops=2 * M * N * K))
-            W.dev_in.append(Xd)
-            W.dev_out.append(Y)
-            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
-            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
     return W
 
 
@@ -354,7 +382,7 @@ def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
     W.dominant = "gemm_fp8_block"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "fp8"
-    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    W.arena(wl)
     wq = {}
     for si, (K, N) in enumerate(wl.KNs):
         Wd = W.dev_bf16(CFG.make_w(wl, N, K, salt=si))
@@ -364,10 +392,10 @@ def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
         for si, (K, N) in enumerate(wl.KNs):
             Wq, sw = wq[si]
             xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
-            Xd = W.dev_bf16(xb)
+            Xd = W.input(xb)
             Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
             sx = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            Y = W.output(M, N)
             desc = L.make_desc(L.FMT_FP8, L.GRAN_BLOCK_1x128, L.GRAN_BLOCK_128x128, Xq, Wq, sx, sw, Y, M=M, N=N, K=K)
             W.keep = getattr(W, "keep", []) + [desc, Wq, sw, Xq, sx, Y]
             W.calls.append(dict(kind="quant_fp8_1x128", M=M, K=K, N=N,
@@ -375,10 +403,6 @@ def build_prefill_block(L, torch, wl=CFG.PREFILL_FP8_BLOCK):
                                 bytes=M * K * 3 + 4 * M * K // 128, flops=0))
             W.calls.append(dict(kind="gemm_fp8_block", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
                                 bytes=(M + N) * K + 2 * M * N, flops=2 * M * N * K))
-            W.dev_in.append(Xd)
-            W.dev_out.append(Y)
-            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
-            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
     return W
 
 
@@ -397,7 +421,7 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
     W.dominant = "gemm_int8"
     W.dominant_bound = "tensor"
     W.dominant_dtype = "int8"
-    W.host_in, W.host_out, W.dev_in, W.dev_out = [], [], [], []
+    W.arena(wl)
     K = wl.KNs[0][0]
     amax = torch.zeros(K, dtype=torch.float32, device="cuda")
     L.lpq_act_absmax_update(W.dev_bf16(CFG.make_calib(wl, K)), amax)
@@ -418,10 +442,10 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
         for si, (K, N) in enumerate(wl.KNs):
             Wq, sw, sm = wq[si]
             xb = CFG.make_x(wl, M, K, salt=mi * 10 + si)
-            Xd = W.dev_bf16(xb)
+            Xd = W.input(xb)
             Xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
             sx = torch.empty((M,), dtype=torch.float32, device="cuda")
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            Y = W.output(M, N)
             desc = L.make_desc(L.FMT_INT8, L.GRAN_ROW, L.GRAN_ROW, Xq, Wq, sx, sw, Y, M=M, N=N, K=K, workspace=ws,
                                flags=flags)
             W.keep = getattr(W, "keep", []) + [desc, Wq, sw, sm, Xq, sx, Y]
@@ -430,10 +454,6 @@ def build_int8(L, torch, wl=CFG.INT8_SMOOTHQUANT):
                                 bytes=M * K * 3 + 4 * M, flops=0))
             W.calls.append(dict(kind="gemm_int8", M=M, K=K, N=N, fn=(lambda d=desc: L.lpq_gemm_scaled(d)),
                                 bytes=(M + N) * K + 4 * (M + N) + 2 * M * N, flops=2 * M * N * K))
-            W.dev_in.append(Xd)
-            W.dev_out.append(Y)
-            W.host_in.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
-            W.host_out.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
     return W
 
 
@@ -574,6 +594,7 @@ def main():
         W.dev_out = [W.dev_out[i // 2] for i in idx]
         W.host_in = [W.host_in[i // 2] for i in idx]
         W.host_out = [W.host_out[i // 2] for i in idx]
+        W.subset = True
         W.config["only"] = args.only
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -727,12 +748,16 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in W.host_out)
     n_e2e = max(3, args.steps // 2)
 
+    # the whole step's activations / outputs as one copy each (per call for a subset)
+    pairs_in = list(zip(W.host_in, W.dev_in)) if W.subset else [(W.hin, W.din)]
+    pairs_out = list(zip(W.host_out, W.dev_out)) if W.subset else [(W.hout, W.dout)]
+
     def e2e_steps():
         for _ in range(n_e2e):
-            for h, d in zip(W.host_in, W.dev_in):
+            for h, d in pairs_in:
                 d.copy_(h, non_blocking=True)
             step()
-            for h, d in zip(W.host_out, W.dev_out):
+            for h, d in pairs_out:
                 h.copy_(d, non_blocking=True)
 
     g2 = capture(e2e_steps) if g_run is not None else None
